@@ -1,0 +1,477 @@
+"""Benchmark of the epilogue-fusion hot path on GB300.
+
+Headline (the JSON line's `value`): fused conv2d + BN + SiLU on the largest
+workload, NHWC bf16 16x64x64x512 -> 512, 7x7, pad 3 (1.684 TFLOP per step),
+through the C ABI with every input resident in HBM, in TFLOP/s.  The same run
+measures the other workloads of the path -- fused bias + GELU on fp16
+[8192, 8192], fused residual + LayerNorm + affine on fp16 [16384, 4096], the
+1x1 conv 32x56x56x256 -> 256 and the tiny 3x3 conv -- each next to the
+unfused chain of our own separate kernels, and reports them under
+`workloads`.
+
+L2: each workload rotates over enough copies of its input/output buffers that
+more than twice the 126 MB L2 is touched between two uses of the same buffer,
+so every timed step reads its inputs from HBM.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch under torch.distributed.run (one process per GPU); each rank
+runs its own replica of the workload (weak scaling, no collective on the data
+path) and rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "conv7x7_16x64x64x512_to512"
+METRIC = "conv+BN+SiLU TFLOP/s (% bf16 peak); fused-chain GB/s (% HBM peak)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 126 * 2**20
+
+
+# ---------------------------------------------------------------- peaks, clocks, traffic
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            p = json.load(open(path))
+            hbm = p.get("hbm_gbs")
+            bf16 = p.get("bf16_tflops")
+            if hbm and bf16:
+                return {"hbm_gbs": float(hbm), "bf16_tflops": float(bf16),
+                        "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained") or bf16),
+                        "source": "of measured"}
+        except Exception:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "of fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) >= 9:
+                self.rows.append([c.strip() for c in row])
+
+    def summary(self) -> dict:
+        rows = getattr(self, "rows", [])
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source has not changed since it was captured (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        t = json.load(open(path)).get(kernel)
+        if not t:
+            return None
+        src = os.path.join(ROOT, "gemm_conv_epilogues_gb300", "csrc", t["source"])
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != t["source_sha256_16"]:
+            return None
+        return float(t["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- workloads
+
+class Runner:
+    """Device buffers of one workload (several rotating sets) and the launch
+    functions of its fused call and unfused chain."""
+
+    def __init__(self, name: str, seed: int):
+        import torch
+        from gemm_conv_epilogues_gb300 import binding as b, synth
+        self.b, self.torch = b, torch
+        self.w = synth.WORKLOADS[name]
+        self.name = name
+        self.inputs = synth.workload_inputs(self.w, seed)
+        d = self.inputs
+        dev = "cuda"
+        up16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16).copy()).to(dev)
+        up = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt).copy()).to(dev)
+        w = self.w
+        if w.kind == "conv":
+            c = w.conv
+            self.shape = b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad)
+            self.M = c.M
+            self.flops = c.flops
+            x_bytes = c.N * c.H * c.W * c.C_in * 2
+            y_bytes = c.M * c.C_out * 2
+            w_bytes = c.C_out * c.K * 2
+            self.alg_bytes = x_bytes + y_bytes + w_bytes + 8 * c.C_out
+            self.unfused_extra = 4 * y_bytes
+            self.h2d, self.d2h = x_bytes, y_bytes
+            self.wt = torch.empty((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device=dev)
+            b.tf_pack_filter_nhwc(up16(d["w_oihw"]), self.wt, c.C_out, c.C_in, c.KH, c.KW)   # load time
+            self.scale, self.bias = up(d["scale"], np.float32), up(d["bias"], np.float32)
+            per_set = x_bytes + y_bytes
+            nsets = max(1, min(8, int(np.ceil(2 * L2_BYTES / per_set)) + 1))
+            x0 = up16(d["x"])
+            self.sets = []
+            for _ in range(nsets):
+                self.sets.append({"x": x0.clone(), "y": torch.empty((c.M, c.C_out), dtype=torch.int16, device=dev)})
+            self.t1 = torch.empty((c.M, c.C_out), dtype=torch.int16, device=dev)
+            self.t2 = torch.empty_like(self.t1)
+            self.host_x = torch.from_numpy(d["x"].view(np.int16).copy()).pin_memory()
+            self.host_y = torch.empty((c.M, c.C_out), dtype=torch.int16).pin_memory()
+        elif w.kind == "bias_gelu":
+            rows, cols = w.rows, w.cols
+            self.flops = 0
+            n = rows * cols
+            self.alg_bytes = 2 * n + 2 * n + 2 * cols
+            self.unfused_extra = 4 * n
+            self.h2d, self.d2h = 2 * n, 2 * n
+            per_set = 4 * n
+            nsets = max(1, int(np.ceil(2 * L2_BYTES / per_set)) + 1)
+            x0 = up(d["x"], np.float16)
+            self.bias = up(d["bias"], np.float16)
+            self.sets = [{"x": x0.clone(), "y": torch.empty_like(x0)} for _ in range(nsets)]
+            self.t = torch.empty_like(x0)
+            self.host_x = torch.from_numpy(d["x"].copy()).pin_memory()
+            self.host_y = torch.empty((rows, cols), dtype=torch.float16).pin_memory()
+        else:
+            rows, hidden = w.rows, w.cols
+            self.flops = 0
+            n = rows * hidden
+            self.alg_bytes = 2 * n * 3 + 8 * hidden
+            self.unfused_extra = 8 * n
+            self.h2d, self.d2h = 4 * n, 2 * n
+            per_set = 6 * n
+            nsets = max(1, int(np.ceil(2 * L2_BYTES / per_set)) + 1)
+            a0, r0 = up(d["act"], np.float16), up(d["res"], np.float16)
+            self.gamma, self.beta = up(d["gamma"], np.float32), up(d["beta"], np.float32)
+            self.sets = [{"a": a0.clone(), "r": r0.clone(), "y": torch.empty_like(a0)} for _ in range(nsets)]
+            self.s = torch.empty_like(a0)
+            self.n = torch.empty_like(a0)
+            self.host_a = torch.from_numpy(d["act"].copy()).pin_memory()
+            self.host_r = torch.from_numpy(d["res"].copy()).pin_memory()
+            self.host_y = torch.empty((rows, hidden), dtype=torch.float16).pin_memory()
+        self.nsets = len(self.sets)
+
+    # one fused call on buffer set i: returns the number of our kernels launched
+    def fused(self, i: int) -> int:
+        b, s, w = self.b, self.sets[i % self.nsets], self.w
+        if w.kind == "conv":
+            b.tf_conv2d_bn_silu(s["x"], self.wt, self.scale, self.bias, s["y"], self.shape)
+        elif w.kind == "bias_gelu":
+            b.tf_bias_gelu(s["x"], self.bias, s["y"], w.rows, w.cols)
+        else:
+            b.tf_residual_layernorm(s["a"], s["r"], self.gamma, self.beta, s["y"], w.rows, w.cols, w.eps)
+        return 1
+
+    def unfused(self, i: int) -> int:
+        b, s, w = self.b, self.sets[i % self.nsets], self.w
+        if w.kind == "conv":
+            c = w.conv
+            b.tf_unfused_conv2d(s["x"], self.wt, self.t1, self.shape)
+            b.tf_unfused_bn(self.t1, self.scale, self.bias, self.t2, c.M, c.C_out)
+            b.tf_unfused_silu(self.t2, s["y"], c.M * c.C_out)
+            return 3
+        if w.kind == "bias_gelu":
+            b.tf_unfused_bias_add(s["x"], self.bias, self.t, w.rows, w.cols)
+            b.tf_unfused_gelu(self.t, s["y"], w.rows * w.cols)
+            return 2
+        b.tf_unfused_residual_add(s["a"], s["r"], self.s, w.rows * w.cols)
+        b.tf_unfused_layernorm(self.s, self.n, w.rows, w.cols, w.eps)
+        b.tf_unfused_affine(self.n, self.gamma, self.beta, s["y"], w.rows, w.cols)
+        return 3
+
+    # end to end through the C ABI from pinned host buffers: H2D of the step's
+    # inputs, the fused call, D2H of the result
+    def e2e(self, i: int) -> int:
+        s = self.sets[i % self.nsets]
+        if self.w.kind == "layernorm":
+            s["a"].copy_(self.host_a, non_blocking=True)
+            s["r"].copy_(self.host_r, non_blocking=True)
+        else:
+            s["x"].copy_(self.host_x, non_blocking=True)
+        k = self.fused(i)
+        self.host_y.copy_(s["y"].view(self.host_y.shape), non_blocking=True)
+        return k
+
+
+def time_loop(fn, steps: int, warmup: int, world: int, clocks=None):
+    """Times exactly `steps` calls of fn(i) with CUDA events on the current
+    stream, bracketed by a barrier and a device synchronise on both sides;
+    returns (max-over-ranks ms per step, kernels launched in the timed region)."""
+    import torch
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    ctx = clocks if clocks is not None else _Null()
+    with ctx:
+        ev0.record(stream)
+        for i in range(steps):
+            launches += fn(warmup + i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1) / steps
+    return max_over_ranks(ms, world), launches
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def roofline(bound, achieved, peak, unit, traffic):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic}
+
+
+# ---------------------------------------------------------------- CPU baseline (the oracle)
+
+def cpu_baseline_conv7x7(target_s: float = 12.0) -> dict:
+    """The fp64 oracle, as it stands, on a sample of output pixels of the 7x7
+    workload (all 512 channels of each), on every host core."""
+    import oracle
+    from gemm_conv_epilogues_gb300 import synth
+    w = synth.WORKLOADS[HEADLINE]
+    c = w.conv
+    d = synth.workload_inputs(w)
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(0)
+    flops_per_point = 2 * c.K
+    # calibrate on a small sample, then size the timed sample to ~target_s
+    pix = rng.integers(0, c.M, 8)
+    pts = (pix[:, None] * c.C_out + np.arange(c.C_out)[None, :]).reshape(-1)
+    t0 = time.perf_counter()
+    oracle.conv2d_bn_silu_points(d["x"], d["w_oihw"], d["scale"], d["bias"], pts, c.stride, c.pad, nthreads=threads)
+    rate = pts.size * flops_per_point / (time.perf_counter() - t0)
+    npix = int(max(16, min(4096, target_s * rate / (flops_per_point * c.C_out))))
+    pix = rng.integers(0, c.M, npix)
+    pts = (pix[:, None] * c.C_out + np.arange(c.C_out)[None, :]).reshape(-1)
+    t0 = time.perf_counter()
+    oracle.conv2d_bn_silu_points(d["x"], d["w_oihw"], d["scale"], d["bias"], pts, c.stride, c.pad, nthreads=threads)
+    dt = time.perf_counter() - t0
+    tflops = pts.size * flops_per_point / dt / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{npix} random output pixels x all {c.C_out} channels of {HEADLINE} "
+                      f"({pts.size * flops_per_point / 1e9:.1f} GFLOP, {dt:.1f} s, fp64 7-loop direct conv)",
+            "seconds": dt}
+
+
+# ---------------------------------------------------------------- main
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    per_step = []
+    for _ in range(args.warmup):
+        cpu_baseline_conv7x7(target_s=1.0)
+    for _ in range(args.steps):
+        per_step.append(cpu_baseline_conv7x7(target_s=max(2.0, 60.0 / max(args.steps, 1))))
+    v = statistics.median(p["value"] for p in per_step)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": statistics.median(p["seconds"] for p in per_step) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": HEADLINE, "note": "bounded sample per step"},
+            "cpu_baseline": {"kind": "oracle", "cores": per_step[0]["cores"], "sample": per_step[0]["sample"],
+                             "value": v, "unit": "TFLOP/s"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-headline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from gemm_conv_epilogues_gb300 import build as gbuild
+    if rank == 0:
+        gbuild.build_library()
+    barrier(world)
+    from gemm_conv_epilogues_gb300 import binding as b
+
+    peaks = load_peaks()
+    head = Runner(HEADLINE, seed=rank)
+    clocks = ClockSampler(local)
+    ms, launches = time_loop(head.fused, args.steps, args.warmup, world, clocks)
+    total_flops = head.flops * world
+    value = total_flops / (ms * 1e-3) / 1e12
+    per_launch_tflops = head.flops / (ms * 1e-3) / 1e12
+    e2e_ms, _ = time_loop(head.e2e, max(5, args.steps // 20), args.warmup, world)
+    e2e_val = total_flops / (e2e_ms * 1e-3) / 1e12
+    rc, word = b.tf_read_device_error()
+    if rc != b.TF_OK:
+        raise SystemExit(f"device error word {word:#x} after the timed region")
+
+    workloads = {}
+    unf_ms, _ = time_loop(head.unfused, max(20, args.steps // 10), args.warmup, world)
+    workloads[HEADLINE] = {
+        "fused": {"ms": ms, "tflops": per_launch_tflops, "gbs": head.alg_bytes / (ms * 1e-3) / 1e9},
+        "unfused_chain": {"ms": unf_ms, "launches": 3, "extra_hbm_bytes": head.unfused_extra},
+        "roofline": roofline("tensor", per_launch_tflops, peaks["bf16_tflops"], "TFLOP/s",
+                             kernel_traffic("conv_umma_kernel")),
+    }
+    del head
+    torch.cuda.empty_cache()
+
+    if not args.only_headline:
+        for name in ["conv1x1_32x56x56x256_to256", "bias_gelu_f16_8192x8192",
+                     "residual_layernorm_f16_16384x4096", "conv3x3_tiny_1x16x16x8_to16"]:
+            r = Runner(name, seed=rank)
+            steps = 200 if r.w.kind != "conv" or r.w.conv.M > 1000 else 2000
+            f_ms, _ = time_loop(r.fused, steps, args.warmup, world)
+            u_ms, _ = time_loop(r.unfused, steps // 2, args.warmup, world)
+            gbs = r.alg_bytes / (f_ms * 1e-3) / 1e9
+            entry = {"fused": {"ms": f_ms, "gbs": gbs, "alg_bytes": r.alg_bytes},
+                     "unfused_chain": {"ms": u_ms, "gbs_of_fused_bytes": r.alg_bytes / (u_ms * 1e-3) / 1e9,
+                                       "extra_hbm_bytes": r.unfused_extra},
+                     "l2": f"{r.nsets} rotating buffer sets"}
+            if r.flops:
+                entry["fused"]["tflops"] = r.flops / (f_ms * 1e-3) / 1e12
+            kname = {"conv": "conv_umma_kernel", "bias_gelu": "bias_gelu_kernel",
+                     "layernorm": "layernorm_kernel"}[r.w.kind]
+            if name.startswith("conv3x3_tiny"):
+                entry["note"] = "launch-latency bound (0.59 MFLOP); reported as latency"
+            else:
+                entry["roofline"] = roofline("hbm", gbs, peaks["hbm_gbs"], "GB/s", kernel_traffic(kname))
+            workloads[name] = entry
+            del r
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_conv7x7()
+        cpu.pop("seconds", None)
+
+    if rank == 0:
+        cs = clocks.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": HEADLINE, "N": 16, "H": 64, "W": 64, "C_in": 512, "C_out": 512, "KH": 7,
+                       "KW": 7, "stride": 1, "pad": 3, "flops_per_step_per_gpu": head_flops(),
+                       "l2": "rotating input/output buffer sets, >2x L2 touched between reuses",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": workloads[HEADLINE]["roofline"],
+            "peak_source": peaks["source"],
+            "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(16 * 64 * 64 * 512 * 2),
+                    "d2h_bytes_per_step": int(16 * 64 * 64 * 512 * 2)},
+            "gpu_launches": launches,
+            "clocks": {"sm_mhz": cs["sm_mhz"], "sm_max_mhz": cs["sm_max_mhz"], "reasons": cs["reasons"]},
+            "workloads": workloads,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def head_flops() -> int:
+    from gemm_conv_epilogues_gb300 import synth
+    return synth.WORKLOADS[HEADLINE].conv.flops
+
+
+if __name__ == "__main__":
+    main()

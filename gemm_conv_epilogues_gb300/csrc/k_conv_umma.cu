@@ -1,0 +1,454 @@
+// Implicit-GEMM conv2d + BatchNorm + SiLU on the 5th-generation tensor cores.
+//
+// GEMM view: M = N*Ho*Wo output pixels, N_gemm = C_out, K = KH*KW*C_in in
+// (kh, kw, ci) order, which is the channels-last (OHWI) filter layout
+// ("When the fusion you want is impossible, fuse into the producer": the
+// filters are packed channels-last once at load time).  The A operand is never
+// materialised: TMA's im2col mode gathers 128 output pixels x 64 channels of
+// the NHWC input for one filter tap straight into shared memory (zero fill at
+// the padding), which is the TMA_LOAD_IM2COL -> UMMA path that page describes;
+// a 1x1 stride-1 unpadded convolution is a plain matrix, loaded as a 2-D tile.
+//
+// Persistent kernel, one CTA per SM, six warps:
+//   warp 0  TMA producer: a ring of 4 shared-memory stages (A 16 KB + B BN*128 B)
+//   warp 1  TMEM allocator and MMA issuer: tcgen05.mma M=128, N=BN, K=16, fp32
+//           accumulators in TMEM, double-buffered so the epilogue of one tile
+//           overlaps the main loop of the next
+//   warps 2-5 epilogue ("Fusing an Epilogue", "The shape of it"): TMEM ->
+//           registers, v = acc*scale[co] + bias[co], v*sigmoid(v), bf16, store.
+//           The per-channel parameters are read inside the kernel, as in the
+//           page's BatchNorm-epilog listing.
+// Every mbarrier wait is bounded (see ptx::mbar_wait); a role that times out
+// sets the device error word and winds down, and the CTA drains its in-flight
+// copies and MMAs before it frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ptx_sm100.cuh"
+#include "tf_internal.h"
+
+namespace tf {
+namespace {
+
+constexpr int BM = 128;            // output pixels per tile (UMMA M)
+constexpr int BK = 64;             // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int UMMA_K = 16;
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+
+template <int BN>
+struct Layout {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int BAR_OFFSET = kStages * STAGE_BYTES;
+    static constexpr int NUM_BARS = 2 * kStages + 5;  // full, empty, tmem full x2, tmem empty x2, drain
+    static constexpr int TOTAL = BAR_OFFSET + NUM_BARS * 8 + 16;
+    static constexpr int ALLOC = TOTAL + 1024;        // slack to align the base to 1024 B
+    static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+};
+
+struct UmmaParams {
+    const float *scale;
+    const float *bias;
+    __nv_bfloat16 *y;
+    uint32_t *err;
+    uint64_t wait_ns;
+    int M, C_out, KW, HoWo, Wo;
+    int stride_h, stride_w, pad_h, pad_w;
+    int num_kb, cblocks, num_n_tiles, num_tiles;
+    int epilogue;
+};
+
+template <int BN, bool IM2COL>
+__global__ void __launch_bounds__(kThreads, 1)
+    conv_umma_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                     const UmmaParams p)
+{
+    using L = Layout<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFFSET);
+    uint64_t *empty = full + kStages;
+    uint64_t *tfull = empty + kStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&tfull[b], 1);
+            ptx::mbar_init(&tempty[b], kEpiWarps * 32);
+        }
+        ptx::mbar_init(drain, 1);
+        ptx::mbar_init_fence();
+        ptx::prefetch_tensormap(&tmap_a);
+        ptx::prefetch_tensormap(&tmap_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, L::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, last_phase = 0;  // per-stage bit masks
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                const int m0 = (tile / p.num_n_tiles) * BM;
+                const int n0 = (tile % p.num_n_tiles) * BN;
+                const int img = m0 / p.HoWo;
+                const int rem = m0 - img * p.HoWo;
+                const int oh = rem / p.Wo, ow = rem - (rem / p.Wo) * p.Wo;
+                const int w_base = ow * p.stride_w - p.pad_w, h_base = oh * p.stride_h - p.pad_h;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+                    uint8_t *a_dst = smem + stage * L::STAGE_BYTES;
+                    uint8_t *b_dst = a_dst + L::A_BYTES;
+                    const int tap = kb / p.cblocks;
+                    const int c0 = (kb - tap * p.cblocks) * BK;
+                    if constexpr (IM2COL) {
+                        const int kh = tap / p.KW, kw = tap - (tap / p.KW) * p.KW;
+                        ptx::tma_load_im2col_4d(a_dst, &tmap_a, &full[stage], c0, w_base, h_base, img,
+                                                (uint16_t)kw, (uint16_t)kh);
+                    } else {
+                        ptx::tma_load_2d(a_dst, &tmap_a, &full[stage], c0, m0);
+                    }
+                    ptx::tma_load_2d(b_dst, &tmap_b, &full[stage], kb * BK, n0);
+                    issued |= 1u << stage;
+                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) atomicOr(p.err, TF_DEVERR_PRODUCER_WAIT);
+            // Every issued copy must have landed before the CTA may exit.
+            for (int s = 0; s < kStages; ++s)
+                if ((issued >> s) & 1u)
+                    if (!ptx::mbar_wait(&full[s], (last_phase >> s) & 1u, p.wait_ns))
+                        atomicOr(p.err, TF_DEVERR_DRAIN_WAIT);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int local = 0;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+                const int b = local & 1;
+                const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
+                if (!ptx::mbar_wait(&tempty[b], acc_phase ^ 1u, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ptx::mbar_wait(&full[stage], phase, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_addr = ptx::smem_u32(smem + stage * L::STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + L::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        ptx::umma_bf16(d_tmem, ptx::sw128_kmajor_desc(a_addr + k * UMMA_K * 2),
+                                       ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2), idesc,
+                                       (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    ptx::umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::umma_commit(&tfull[b]);  // accumulator complete
+            }
+            if (!ok) atomicOr(p.err, TF_DEVERR_MMA_WAIT);
+            ptx::umma_commit(drain);
+            if (!ptx::mbar_wait(drain, 0, p.wait_ns)) atomicOr(p.err, TF_DEVERR_DRAIN_WAIT);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
+        const int row = q * 32 + lane;
+        int local = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+            const int m0 = (tile / p.num_n_tiles) * BM;
+            const int n0 = (tile % p.num_n_tiles) * BN;
+            const int b = local & 1;
+            const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
+            const bool got = ptx::mbar_wait(&tfull[b], acc_phase, p.wait_ns);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const int m = m0 + row;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
+            __nv_bfloat16 *yrow = p.y + (int64_t)m * p.C_out + n0;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                ptx::tmem_ld_wait();
+                if (m < p.M) {
+                    float v[32];
+                    if (p.epilogue) {
+                        const float4 *sc = reinterpret_cast<const float4 *>(p.scale + n0 + c * 32);
+                        const float4 *bi = reinterpret_cast<const float4 *>(p.bias + n0 + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 s4 = __ldg(sc + j), b4 = __ldg(bi + j);
+                            v[4 * j + 0] = silu_f32(fmaf(__uint_as_float(r[4 * j + 0]), s4.x, b4.x));
+                            v[4 * j + 1] = silu_f32(fmaf(__uint_as_float(r[4 * j + 1]), s4.y, b4.y));
+                            v[4 * j + 2] = silu_f32(fmaf(__uint_as_float(r[4 * j + 2]), s4.z, b4.z));
+                            v[4 * j + 3] = silu_f32(fmaf(__uint_as_float(r[4 * j + 3]), s4.w, b4.w));
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 o;
+                        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
+                        dst[j] = o;
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&tempty[b]);
+        }
+        if (!ok && lane == 0) atomicOr(p.err, TF_DEVERR_EPILOGUE_WAIT);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+using EncodeIm2colFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                    const cuuint64_t *, const int *, const int *, cuuint32_t, cuuint32_t,
+                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+template <typename Fn>
+Fn driver_fn(const char *name)
+{
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(fn);
+}
+
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = driver_fn<EncodeTiledFn>("cuTensorMapEncodeTiled");
+    return fn;
+}
+
+EncodeIm2colFn encode_im2col()
+{
+    static EncodeIm2colFn fn = driver_fn<EncodeIm2colFn>("cuTensorMapEncodeIm2col");
+    return fn;
+}
+
+int pick_bn(int C_out)
+{
+    if (C_out % 256 == 0) return 256;
+    if (C_out % 128 == 0) return 128;
+    if (C_out % 64 == 0) return 64;
+    if (C_out % 32 == 0) return 32;
+    return 0;
+}
+
+bool is_plain_gemm(const tf_conv_shape &s)
+{
+    return s.KH == 1 && s.KW == 1 && s.stride_h == 1 && s.stride_w == 1 && s.pad_h == 0 && s.pad_w == 0;
+}
+
+// Upper corner of the im2col bounding box relative to the far edge, chosen so
+// that the box, traversed with the conv stride, holds exactly Wo (Ho) base
+// positions ow*stride - pad.
+int upper_corner(int in, int out, int stride, int pad) { return (out - 1) * stride - pad - (in - 1); }
+
+template <int BN, bool IM2COL>
+cudaError_t launch_bn(const ConvArgs &a, const CUtensorMap &ta, const CUtensorMap &tb, const UmmaParams &p,
+                      cudaStream_t st)
+{
+    using L = Layout<BN>;
+    // Per-function, per-device attribute; cheap enough to set on every launch.
+    cudaError_t e = cudaFuncSetAttribute(conv_umma_kernel<BN, IM2COL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
+    conv_umma_kernel<BN, IM2COL><<<grid, kThreads, L::ALLOC, st>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+template <bool IM2COL>
+cudaError_t launch_im(int bn, const ConvArgs &a, const CUtensorMap &ta, const CUtensorMap &tb,
+                      const UmmaParams &p, cudaStream_t st)
+{
+    switch (bn) {
+    case 256: return launch_bn<256, IM2COL>(a, ta, tb, p, st);
+    case 128: return launch_bn<128, IM2COL>(a, ta, tb, p, st);
+    case 64: return launch_bn<64, IM2COL>(a, ta, tb, p, st);
+    case 32: return launch_bn<32, IM2COL>(a, ta, tb, p, st);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace
+
+bool conv_umma_supports(const tf_conv_shape &s, int Ho, int Wo)
+{
+    if (s.C_in % BK != 0 || pick_bn(s.C_out) == 0) return false;
+    if ((int64_t)s.N * Ho * Wo >= (int64_t)1 << 31) return false;
+    if (is_plain_gemm(s)) return true;
+    // im2col geometry: this build takes symmetric geometry only (equal kernel
+    // extent, stride and padding along H and W), so the two spatial entries of
+    // the bounding-box corners are equal.
+    if (s.KH != s.KW || s.stride_h != s.stride_w || s.pad_h != s.pad_w) return false;
+    if (s.stride_w > 8 || s.KW > 256) return false;
+    const int lw = -s.pad_w, uw = upper_corner(s.W, Wo, s.stride_w, s.pad_w);
+    const int lh = -s.pad_h, uh = upper_corner(s.H, Ho, s.stride_h, s.pad_h);
+    if (lw != lh || uw != uh) return false;
+    if (lw < -128 || lw > 127 || uw < -128 || uw > 127) return false;
+    return true;
+}
+
+cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
+{
+    const tf_conv_shape &s = a.s;
+    if (!conv_umma_supports(s, a.Ho, a.Wo)) return cudaErrorNotSupported;
+    EncodeTiledFn tiled = encode_tiled();
+    if (!tiled) return cudaErrorNotSupported;
+    const int bn = pick_bn(s.C_out);
+    const int64_t M = (int64_t)s.N * a.Ho * a.Wo;
+    const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
+
+    CUtensorMap ta, tb;
+    {   // B: packed filters as a [C_out][K] K-major matrix
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)s.C_out};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {BK, (cuuint32_t)bn};
+        const cuuint32_t estr[2] = {1, 1};
+        if (tiled(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.w), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const bool im2col = !is_plain_gemm(s);
+    if (!im2col) {   // A: the input itself is the [M][C_in] matrix
+        const cuuint64_t dims[2] = {(cuuint64_t)s.C_in, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)s.C_in * 2};
+        const cuuint32_t box[2] = {BK, BM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (tiled(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.x), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else {         // A: im2col view of the NHWC input
+        EncodeIm2colFn enc = encode_im2col();
+        if (!enc) return cudaErrorNotSupported;
+        const cuuint64_t dims[4] = {(cuuint64_t)s.C_in, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)s.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)s.C_in * 2, (cuuint64_t)s.W * s.C_in * 2,
+                                       (cuuint64_t)s.H * s.W * s.C_in * 2};
+        const int lower[2] = {-s.pad_w, -s.pad_h};
+        const int upper[2] = {upper_corner(s.W, a.Wo, s.stride_w, s.pad_w), upper_corner(s.H, a.Ho, s.stride_h, s.pad_h)};
+        const cuuint32_t estr[4] = {1, (cuuint32_t)s.stride_w, (cuuint32_t)s.stride_h, 1};
+        if (enc(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(a.x), dims, strides, lower, upper, BK,
+                BM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+
+    UmmaParams p;
+    p.scale = a.scale;
+    p.bias = a.bias;
+    p.y = reinterpret_cast<__nv_bfloat16 *>(a.y);
+    p.err = device_error_word();
+    p.wait_ns = wait_limit_ns();
+    p.M = (int)M;
+    p.C_out = s.C_out;
+    p.KW = s.KW;
+    p.HoWo = a.Ho * a.Wo;
+    p.Wo = a.Wo;
+    p.stride_h = s.stride_h;
+    p.stride_w = s.stride_w;
+    p.pad_h = s.pad_h;
+    p.pad_w = s.pad_w;
+    p.cblocks = s.C_in / BK;
+    p.num_kb = (int)(K / BK);
+    p.num_n_tiles = s.C_out / bn;
+    p.num_tiles = (int)((M + BM - 1) / BM) * p.num_n_tiles;
+    p.epilogue = a.epilogue;
+    if (p.err == nullptr) return cudaErrorInitializationError;
+    return im2col ? launch_im<true>(bn, a, ta, tb, p, st) : launch_im<false>(bn, a, ta, tb, p, st);
+}
+
+// ---------------------------------------------------------------- wait probe
+
+namespace {
+__global__ void wait_probe_kernel(uint32_t *err, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::mbar_init_fence();
+    }
+    __syncthreads();
+    // Nothing ever arrives on `bar`: phase 0 never completes, the wait gives up.
+    if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0, limit_ns)) atomicOr(err, TF_DEVERR_PROBE_WAIT);
+}
+}  // namespace
+
+cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t st)
+{
+    uint32_t *err = device_error_word();
+    if (err == nullptr) return cudaErrorInitializationError;
+    wait_probe_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace tf

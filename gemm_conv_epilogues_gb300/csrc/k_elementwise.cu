@@ -1,0 +1,257 @@
+// Memory-bound kernels: the channels-last filter pack, fused bias + GELU and
+// the separate elementwise kernels of the unfused comparison chains.
+//
+// Every streaming kernel moves 16 bytes per thread per access (eight fp16 or
+// bf16 values), reads with the non-coherent streaming path and writes with
+// evict-first stores, and runs a grid of a few CTAs per SM that strides over
+// the tensor, so each thread keeps several independent 16-byte loads in flight.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tf_internal.h"
+
+namespace tf {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;  // independent 16-byte vectors per thread per iteration
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream(void *p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void h8_to_f(const uint4 &v, float (&f)[8])
+{
+    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __half22float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 f_to_h8(const float (&f)[8])
+{
+    uint4 v;
+    __half2 *h = reinterpret_cast<__half2 *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+    return v;
+}
+
+__device__ __forceinline__ void b8_to_f(const uint4 &v, float (&f)[8])
+{
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 f_to_b8(const float (&f)[8])
+{
+    uint4 v;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return v;
+}
+
+// Grid size for a grid-stride kernel over `nvec` 16-byte vectors: enough CTAs
+// to fill every SM several times, never more than the work needs.
+unsigned grid_for(int64_t nvec)
+{
+    int64_t per_cta = (int64_t)kThreads * kUnroll;
+    int64_t need = (nvec + per_cta - 1) / per_cta;
+    int64_t cap = (int64_t)sm_count() * 8;
+    int64_t g = need < cap ? need : cap;
+    return (unsigned)(g > 0 ? g : 1);
+}
+
+// ---------------------------------------------------------------- bias + GELU
+
+// y = GELU(x + bias[col]).  cols % 8 == 0, so a 16-byte vector never crosses a
+// row and its eight bias values are bias[col .. col+7].
+__global__ void __launch_bounds__(kThreads) bias_gelu_kernel(const uint4 *__restrict__ x,
+                                                             const uint4 *__restrict__ bias,
+                                                             uint4 *__restrict__ y, int64_t nvec,
+                                                             int64_t cvec)
+{
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
+        uint4 xv[kUnroll], bv[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) xv[u] = ld_stream(x + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) bv[u] = __ldg(bias + (i + u * stride) % cvec);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            float a[8], b[8];
+            h8_to_f(xv[u], a);
+            h8_to_f(bv[u], b);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) a[k] = gelu_f32(a[k] + b[k]);
+            st_stream(y + i + u * stride, f_to_h8(a));
+        }
+    }
+    for (; i < nvec; i += stride) {
+        float a[8], b[8];
+        h8_to_f(ld_stream(x + i), a);
+        h8_to_f(__ldg(bias + i % cvec), b);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) a[k] = gelu_f32(a[k] + b[k]);
+        st_stream(y + i, f_to_h8(a));
+    }
+}
+
+// ---------------------------------------------------------------- unfused pieces
+
+enum class Op { BiasAddF16, GeluF16, ResidualAddF16, BnBf16, SiluBf16 };
+
+// One elementwise step of an unfused chain: reads one (or two) tensors,
+// writes one, all in the storage type of the chain.
+template <Op OP>
+__global__ void __launch_bounds__(kThreads) chain_kernel(const uint4 *__restrict__ a,
+                                                         const void *__restrict__ b,
+                                                         const float *__restrict__ scale,
+                                                         uint4 *__restrict__ out, int64_t nvec,
+                                                         int64_t cvec)
+{
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nvec; i += stride) {
+        float f[8];
+        if constexpr (OP == Op::BiasAddF16) {
+            float g[8];
+            h8_to_f(ld_stream(a + i), f);
+            h8_to_f(__ldg(reinterpret_cast<const uint4 *>(b) + i % cvec), g);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] += g[k];
+            st_stream(out + i, f_to_h8(f));
+        } else if constexpr (OP == Op::GeluF16) {
+            h8_to_f(ld_stream(a + i), f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = gelu_f32(f[k]);
+            st_stream(out + i, f_to_h8(f));
+        } else if constexpr (OP == Op::ResidualAddF16) {
+            float g[8];
+            h8_to_f(ld_stream(a + i), f);
+            h8_to_f(ld_stream(reinterpret_cast<const uint4 *>(b) + i), g);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] += g[k];
+            st_stream(out + i, f_to_h8(f));
+        } else if constexpr (OP == Op::BnBf16) {
+            // b = bias, scale = scale, per channel c = (8*i) % C
+            b8_to_f(ld_stream(a + i), f);
+            const int64_t c0 = (i % cvec) * 8;
+            const float *bias = reinterpret_cast<const float *>(b);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = f[k] * __ldg(scale + c0 + k) + __ldg(bias + c0 + k);
+            st_stream(out + i, f_to_b8(f));
+        } else {
+            b8_to_f(ld_stream(a + i), f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = silu_f32(f[k]);
+            st_stream(out + i, f_to_b8(f));
+        }
+    }
+}
+
+template <Op OP>
+cudaError_t launch_chain(const void *a, const void *b, const float *scale, void *out, int64_t n,
+                         int64_t cols, cudaStream_t st)
+{
+    const int64_t nvec = n / 8;
+    const unsigned grid = grid_for(nvec);
+    chain_kernel<OP><<<grid, kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(a), b, scale,
+                                                 reinterpret_cast<uint4 *>(out), nvec, cols / 8);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- filter pack
+
+// w_ohwi[co][kh][kw][ci] = w_oihw[co][ci][kh][kw].  One thread per output
+// word, so the writes are contiguous; runs once at load time.
+__global__ void pack_filter_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
+                                   int C_out, int C_in, int KH, int KW)
+{
+    const int64_t total = (int64_t)C_out * C_in * KH * KW;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < total; o += stride) {
+        int64_t r = o;
+        const int ci = (int)(r % C_in);
+        r /= C_in;
+        const int kw = (int)(r % KW);
+        r /= KW;
+        const int kh = (int)(r % KH);
+        const int64_t co = r / KH;
+        dst[o] = src[((co * C_in + ci) * KH + kh) * KW + kw];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bias_gelu(const void *x, const void *bias, void *y, int64_t rows, int64_t cols,
+                             cudaStream_t st)
+{
+    const int64_t nvec = rows * cols / 8;
+    bias_gelu_kernel<<<grid_for(nvec), kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(x),
+                                                          reinterpret_cast<const uint4 *>(bias),
+                                                          reinterpret_cast<uint4 *>(y), nvec, cols / 8);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unfused_bias_add(const void *x, const void *bias, void *t, int64_t rows,
+                                    int64_t cols, cudaStream_t st)
+{
+    return launch_chain<Op::BiasAddF16>(x, bias, nullptr, t, rows * cols, cols, st);
+}
+
+cudaError_t launch_unfused_gelu(const void *t, void *y, int64_t n, cudaStream_t st)
+{
+    return launch_chain<Op::GeluF16>(t, nullptr, nullptr, y, n, 8, st);
+}
+
+cudaError_t launch_unfused_residual_add(const void *a, const void *r, void *s, int64_t n,
+                                        cudaStream_t st)
+{
+    return launch_chain<Op::ResidualAddF16>(a, r, nullptr, s, n, 8, st);
+}
+
+cudaError_t launch_unfused_bn(const void *t1, const float *scale, const float *bias, void *t2,
+                              int64_t M, int64_t C, cudaStream_t st)
+{
+    return launch_chain<Op::BnBf16>(t1, bias, scale, t2, M * C, C, st);
+}
+
+cudaError_t launch_unfused_silu(const void *t2, void *y, int64_t n, cudaStream_t st)
+{
+    return launch_chain<Op::SiluBf16>(t2, nullptr, nullptr, y, n, 8, st);
+}
+
+cudaError_t launch_pack_filter(const void *w_oihw, void *w_ohwi, int C_out, int C_in, int KH, int KW,
+                               cudaStream_t st)
+{
+    const int64_t total = (int64_t)C_out * C_in * KH * KW;
+    int64_t g = (total + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (g > cap) g = cap;
+    pack_filter_kernel<<<(unsigned)g, 256, 0, st>>>(reinterpret_cast<const uint16_t *>(w_oihw),
+                                                    reinterpret_cast<uint16_t *>(w_ohwi), C_out, C_in, KH, KW);
+    return cudaGetLastError();
+}
+
+}  // namespace tf

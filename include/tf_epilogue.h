@@ -1,0 +1,208 @@
+/*
+ * tf_epilogue.h -- C ABI of the GB300 (sm_103a) epilogue-fusion library
+ * (libtf_epilogue.so).
+ *
+ * Epilogue fusion: a producer's output tile gets its cheap per-element work
+ * (per-channel BatchNorm scale/bias and SiLU, bias + GELU, residual +
+ * LayerNorm + affine) while it is still on chip, and is written to HBM once.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  The library
+ *    allocates no device memory in any call.  Outputs must not alias inputs.
+ *  - Every call is asynchronous on the given stream (a cudaStream_t; NULL is
+ *    the legacy default stream) and never synchronises the device.
+ *  - Arguments are validated on the host before anything is launched:
+ *      TF_ERR_INVALID_ARG  a required pointer is NULL or a size is <= 0
+ *                          (or the shape has an empty output);
+ *      TF_ERR_UNSUPPORTED  a layout or alignment this build has no kernel
+ *                          for (e.g. a pointer not 16-byte aligned, a row
+ *                          length not a multiple of 8);
+ *      TF_ERR_CUDA         the CUDA runtime refused the launch;
+ *      TF_ERR_TIMEOUT      a bounded device-side wait ran out (reported by
+ *                          tf_read_device_error after the stream completes).
+ *    Nothing is launched when a call returns an error before TF_ERR_CUDA.
+ *    There is no CPU fallback: an unsupported case is an error.
+ *  - No C++ exception crosses this boundary.
+ *  - Storage types: bf16 = bfloat16, fp16 = IEEE binary16, both passed as
+ *    void pointers; fp32 parameters as float pointers.  Arithmetic is fp32.
+ *    Every cast to bf16/fp16 rounds to nearest even.
+ */
+#ifndef TF_EPILOGUE_H
+#define TF_EPILOGUE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared here so that the header needs no CUDA include. */
+typedef struct CUstream_st *tf_stream_t;
+
+typedef enum {
+    TF_OK = 0,
+    TF_ERR_INVALID_ARG = 1,
+    TF_ERR_UNSUPPORTED = 2,
+    TF_ERR_CUDA = 3,
+    TF_ERR_TIMEOUT = 4
+} tf_status;
+
+/* Convolution geometry.  Input x is NHWC [N][H][W][C_in]; output y is NHWC
+ * [N][Ho][Wo][C_out] with Ho = (H + 2*pad_h - KH)/stride_h + 1 and
+ * Wo = (W + 2*pad_w - KW)/stride_w + 1 (floor division); taps outside the
+ * input read zero. */
+typedef struct {
+    int N, H, W, C_in, C_out, KH, KW;
+    int stride_h, stride_w, pad_h, pad_w;
+} tf_conv_shape;
+
+/* Convolution kernels (see tf_conv2d_bn_silu_variant). */
+typedef enum {
+    TF_CONV_AUTO = -1,   /* dispatch by shape */
+    TF_CONV_DIRECT = 0,  /* one output element per thread, CUDA-core fp32 */
+    TF_CONV_TILED = 1,   /* output-space tiles with a shared-memory halo, CUDA cores */
+    TF_CONV_UMMA = 2     /* implicit GEMM: TMA im2col -> tcgen05.mma -> TMEM -> fused epilogue */
+} tf_conv_variant;
+
+/* Human-readable name of a status code (static storage). */
+const char *tf_status_string(int status);
+
+/* ---------------------------------------------------------------- filters */
+
+/* Pack convolution filters channels-last, once, at load time.
+ * "When the fusion you want is impossible, fuse into the producer"
+ * (skandtandon.pages.dev), closing paragraphs: the filters were stored in the
+ * wrong layout, so conversions wrapped every convolution; storing them
+ * channels-last once at load time removed them with bit-identical output.
+ *   w_oihw : bf16 [C_out][C_in][KH][KW]   (read)
+ *   w_ohwi : bf16 [C_out][KH][KW][C_in]   (written; a pure permutation)
+ * Both device pointers, no alignment requirement.  Sizes must be > 0. */
+int tf_pack_filter_nhwc(const void *w_oihw, void *w_ohwi,
+                        int C_out, int C_in, int KH, int KW, tf_stream_t stream);
+
+/* ---------------------------------------------------------------- conv */
+
+/* Fused conv2d + per-channel BatchNorm (scale, bias) + SiLU.
+ * "Fusing an Epilogue" (docs.teenygrad.org), "The shape of it" and the
+ * BatchNorm-epilog listing: after the K loop the accumulator tile gets
+ * acc*bn_scale + bn_bias and then acc*sigmoid(acc) before the single store;
+ * the per-channel parameters are loaded inside the same kernel, masked at
+ * the C_out edge.
+ *   x      : bf16 NHWC [N][H][W][C_in]
+ *   w_ohwi : bf16 [C_out][KH][KW][C_in] (from tf_pack_filter_nhwc)
+ *   scale, bias : fp32 [C_out] (BatchNorm already folded into a scale and a
+ *            bias per output channel; no running statistics, no eps here)
+ *   y      : bf16 NHWC [N][Ho][Wo][C_out]
+ * y[n][oh][ow][co] = SiLU(acc*scale[co] + bias[co]) with
+ * acc = sum_{kh,kw,ci} x[n][oh*sh-ph+kh][ow*sw-pw+kw][ci] * w[co][kh][kw][ci]
+ * accumulated in fp32.  Requires C_in % 8 == 0 and 16-byte aligned x, w, y.
+ * The kernel is chosen by shape (see tf_conv2d_bn_silu_select). */
+int tf_conv2d_bn_silu(const void *x, const void *w_ohwi, const float *scale, const float *bias,
+                      void *y, const tf_conv_shape *shape, tf_stream_t stream);
+
+/* Same as tf_conv2d_bn_silu with the kernel forced (TF_CONV_*).  Returns
+ * TF_ERR_UNSUPPORTED when the forced kernel cannot take the shape
+ * (TF_CONV_UMMA needs C_in % 64 == 0 and C_out % 16 == 0). */
+int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *scale,
+                              const float *bias, void *y, const tf_conv_shape *shape,
+                              int variant, tf_stream_t stream);
+
+/* The kernel tf_conv2d_bn_silu would run for this shape (host only, launches
+ * nothing), or a negative tf_status value when the shape is rejected.
+ * "Fusing an Epilogue", "Three kernels for one operation": the lowering picks
+ * one of three kernels by shape with hand-chosen thresholds; this build's
+ * thresholds are measured on GB300. */
+int tf_conv2d_bn_silu_select(const tf_conv_shape *shape);
+
+/* ---------------------------------------------------------------- bias + GELU */
+
+/* y[i][j] = GELU(x[i][j] + bias[j]), GELU with the erf definition
+ * s * Phi(s).  "Costs and benefits of kernel fusion"
+ * (intro-to-ai-systems-performance), opening example: the fused kernel
+ * computes the addition and GELU per value and writes y once instead of
+ * materialising the fp16 x + bias tensor.
+ *   x, y : fp16 [rows][cols] row-major;  bias : fp16 [cols], broadcast over rows.
+ * Requires cols % 8 == 0 and 16-byte aligned x, bias, y. */
+int tf_bias_gelu(const void *x, const void *bias, void *y, int64_t rows, int64_t cols,
+                 tf_stream_t stream);
+
+/* ---------------------------------------------------------------- residual + LN */
+
+/* y = LayerNorm(act + res) * gamma + beta, one HBM pass.  "Costs and benefits
+ * of kernel fusion", "Worked example: Fusing a residual and normalization
+ * chain": load activation and residual once, compute the row statistics,
+ * normalise, apply scale and bias, write the final output.
+ *   act, res, y : fp16 [rows][hidden];  gamma, beta : fp32 [hidden]
+ * mean and biased variance of s = act + res per row, computed in fp32 from
+ * registers in two passes (s is never written); y = (s - mean) /
+ * sqrt(var + eps) * gamma + beta.  Requires hidden % 8 == 0,
+ * hidden <= 16384, 16-byte aligned pointers, eps >= 0. */
+int tf_residual_layernorm(const void *act, const void *res, const float *gamma, const float *beta,
+                          void *y, int64_t rows, int64_t hidden, float eps, tf_stream_t stream);
+
+/* ---------------------------------------------------------------- unfused chains */
+
+/* The separate kernels that the fused calls replace, for the traffic and time
+ * comparison ("Fusing an Epilogue", "The problem": conv writes t1, batchnorm
+ * reads t1 and writes t2, silu reads t2 and writes y; "Costs and benefits of
+ * kernel fusion": the eager x + bias then GELU pair, and the eager residual
+ * add, LayerNorm and scale-and-bias kernels).  Each materialises its result
+ * in HBM in the storage type given.  Same validation rules as above. */
+
+/* t1 = conv(x, w) in bf16 (no epilogue), same kernels and shape rules as
+ * tf_conv2d_bn_silu_variant. */
+int tf_unfused_conv2d(const void *x, const void *w_ohwi, void *t1, const tf_conv_shape *shape,
+                      int variant, tf_stream_t stream);
+/* t2[m][c] = t1[m][c]*scale[c] + bias[c]; bf16 [M][C], C % 8 == 0. */
+int tf_unfused_bn(const void *t1, const float *scale, const float *bias, void *t2,
+                  int64_t M, int64_t C, tf_stream_t stream);
+/* y = t2 * sigmoid(t2); bf16, n % 8 == 0. */
+int tf_unfused_silu(const void *t2, void *y, int64_t n, tf_stream_t stream);
+/* t[i][j] = x[i][j] + bias[j]; fp16, cols % 8 == 0. */
+int tf_unfused_bias_add(const void *x, const void *bias, void *t, int64_t rows, int64_t cols,
+                        tf_stream_t stream);
+/* y = GELU(t); fp16, n % 8 == 0. */
+int tf_unfused_gelu(const void *t, void *y, int64_t n, tf_stream_t stream);
+/* s = act + res; fp16, n % 8 == 0. */
+int tf_unfused_residual_add(const void *act, const void *res, void *s, int64_t n,
+                            tf_stream_t stream);
+/* nrm = (s - mean)/sqrt(var + eps) per row, no affine; fp16 in and out. */
+int tf_unfused_layernorm(const void *s, void *nrm, int64_t rows, int64_t hidden, float eps,
+                         tf_stream_t stream);
+/* y[i][j] = nrm[i][j]*gamma[j] + beta[j]; fp16 in and out, fp32 gamma/beta. */
+int tf_unfused_affine(const void *nrm, const float *gamma, const float *beta, void *y,
+                      int64_t rows, int64_t hidden, tf_stream_t stream);
+
+/* ---------------------------------------------------------------- device waits */
+
+/* Every spin-wait inside the library's kernels (mbarrier waits of the
+ * tcgen05 pipeline) gives up after this many nanoseconds of %globaltimer,
+ * records TF_DEVERR_* in a device error word and lets the kernel finish
+ * cleanly.  Default 2e9 (2 s).  Host-side setting, applies to later launches. */
+void tf_set_wait_limit_ns(uint64_t limit_ns);
+uint64_t tf_get_wait_limit_ns(void);
+
+/* Bits of the device error word. */
+#define TF_DEVERR_PRODUCER_WAIT 0x1u  /* TMA producer: smem stage never freed */
+#define TF_DEVERR_MMA_WAIT 0x2u       /* MMA issuer: operands or accumulator never ready */
+#define TF_DEVERR_EPILOGUE_WAIT 0x4u  /* epilogue: accumulator never committed */
+#define TF_DEVERR_DRAIN_WAIT 0x8u     /* in-flight copies/MMAs not drained on exit */
+#define TF_DEVERR_PROBE_WAIT 0x10u    /* tf_wait_probe: the expected time-out */
+
+/* Synchronises the current device, copies the device error word of the
+ * current device into *word (may be NULL), clears it, and returns TF_OK if it
+ * was zero, TF_ERR_TIMEOUT if a wait gave up, TF_ERR_CUDA if the runtime
+ * failed.  Not for use inside stream capture. */
+int tf_read_device_error(uint32_t *word);
+
+/* Launches one small kernel that waits, with the given limit, on an mbarrier
+ * that nothing ever arrives on; it gives up, sets TF_DEVERR_PROBE_WAIT and
+ * returns.  Exercises the time-out path without disturbing the GPU. */
+int tf_wait_probe(uint64_t limit_ns, tf_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TF_EPILOGUE_H */

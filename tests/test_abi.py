@@ -1,0 +1,99 @@
+"""The C-ABI library builds, loads and exports every declared entry point, and
+rejects bad arguments on the host before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tf_epilogue.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(tf_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("tf_pack_filter_nhwc", "tf_conv2d_bn_silu", "tf_bias_gelu", "tf_residual_layernorm"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(native_lib):
+    from gemm_conv_epilogues_gb300 import binding
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (tf_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(native_lib, n)
+
+
+def test_status_strings(native_lib):
+    from gemm_conv_epilogues_gb300 import binding as b
+    assert b.status_string(0) == "TF_OK"
+    for s in (1, 2, 3, 4):
+        assert b.status_string(s).startswith("TF_ERR_")
+
+
+def test_wait_limit_round_trip(native_lib):
+    from gemm_conv_epilogues_gb300 import binding as b
+    old = b.tf_get_wait_limit_ns()
+    try:
+        b.tf_set_wait_limit_ns(12345)
+        assert b.tf_get_wait_limit_ns() == 12345
+    finally:
+        b.tf_set_wait_limit_ns(old)
+
+
+def test_host_validation_rejects_before_launch(native_lib):
+    from gemm_conv_epilogues_gb300 import binding as b
+    S = b.TF_ERR_INVALID_ARG
+    U = b.TF_ERR_UNSUPPORTED
+    p16 = 1 << 20           # a 16-byte aligned fake address; never dereferenced on these paths
+    odd = p16 + 2
+    shape = b.conv_shape(1, 16, 16, 8, 16, 3, 3, (1, 1), (1, 1))
+    assert b.tf_conv2d_bn_silu(None, p16, p16, p16, p16, shape, 0, check=False) == S
+    assert b.tf_conv2d_bn_silu(p16, p16, None, p16, p16, shape, 0, check=False) == S
+    assert b.tf_conv2d_bn_silu(odd, p16, p16, p16, p16, shape, 0, check=False) == U
+    bad = b.conv_shape(1, 16, 16, 12, 16, 3, 3, (1, 1), (1, 1))          # C_in % 8 != 0
+    assert b.tf_conv2d_bn_silu(p16, p16, p16, p16, p16, bad, 0, check=False) == U
+    empty = b.conv_shape(1, 2, 2, 8, 16, 5, 5, (1, 1), (0, 0))           # no output pixel
+    assert b.tf_conv2d_bn_silu(p16, p16, p16, p16, p16, empty, 0, check=False) == S
+    zero = b.conv_shape(0, 16, 16, 8, 16, 3, 3, (1, 1), (1, 1))
+    assert b.tf_conv2d_bn_silu(p16, p16, p16, p16, p16, zero, 0, check=False) == S
+    assert b.tf_conv2d_bn_silu_variant(p16, p16, p16, p16, p16, shape, 7, 0, check=False) == S
+    # the tensor-core kernel needs C_in % 64 == 0
+    assert b.tf_conv2d_bn_silu_variant(p16, p16, p16, p16, p16, shape, b.TF_CONV_UMMA, 0, check=False) == U
+    assert b.tf_bias_gelu(p16, p16, p16, 0, 8, 0, check=False) == S
+    assert b.tf_bias_gelu(p16, None, p16, 4, 8, 0, check=False) == S
+    assert b.tf_bias_gelu(p16, p16, p16, 4, 12, 0, check=False) == U
+    assert b.tf_bias_gelu(p16, p16, odd, 4, 8, 0, check=False) == U
+    assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 0, 1e-5, 0, check=False) == S
+    assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 8, -1.0, 0, check=False) == S
+    assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 20, 1e-5, 0, check=False) == U
+    assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 32768, 1e-5, 0, check=False) == U
+    assert b.tf_pack_filter_nhwc(None, p16, 4, 4, 3, 3, 0, check=False) == S
+    assert b.tf_pack_filter_nhwc(p16, p16, 0, 4, 3, 3, 0, check=False) == S
+    assert b.tf_unfused_bn(p16, p16, p16, p16, 4, 12, 0, check=False) == U
+    assert b.tf_unfused_silu(p16, p16, 0, 0, check=False) == S
+    assert b.tf_unfused_gelu(p16, odd, 8, 0, check=False) == U
+    assert b.tf_unfused_residual_add(p16, p16, p16, 12, 0, check=False) == U
+    assert b.tf_unfused_layernorm(p16, p16, 2, 10, 1e-5, 0, check=False) == U
+    assert b.tf_unfused_affine(p16, p16, p16, None, 2, 8, 0, check=False) == S
+
+
+def test_dispatch_selects_by_shape(native_lib):
+    from gemm_conv_epilogues_gb300 import binding as b, synth
+    w = synth.WORKLOADS
+    sel = lambda c: b.tf_conv2d_bn_silu_select(b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad))
+    assert sel(w["conv3x3_tiny_1x16x16x8_to16"].conv) == b.TF_CONV_DIRECT
+    assert sel(w["conv1x1_32x56x56x256_to256"].conv) == b.TF_CONV_UMMA
+    assert sel(w["conv7x7_16x64x64x512_to512"].conv) == b.TF_CONV_UMMA
+    # shapes the tensor-core kernel cannot take go to the CUDA-core kernels
+    assert sel(synth.ConvShape(8, 32, 32, 24, 48, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
+    assert b.tf_conv2d_bn_silu_select(b.conv_shape(1, 2, 2, 8, 16, 5, 5)) == -b.TF_ERR_INVALID_ARG

@@ -1,0 +1,262 @@
+"""GPU parity: every kernel behind the C ABI against the fp64 oracle on the
+same seeded input bits.
+
+Tolerances:
+  conv (bf16 out)       |gpu - ref| <= 1e-2 + 1e-2*|ref|
+  bias + GELU (fp16)    <= 2 fp16 ulp from the oracle rounded to fp16
+  LayerNorm (fp16)      |gpu - ref| <= 1e-2
+  filter pack           bit-identical
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_conv_epilogues_gb300 import synth
+from helpers import (bf16_to_f64, conv_sample_points, dev_f16, dev_f32, dev_u16, f16_ulp_distance,
+                     host_u16)
+
+pytestmark = pytest.mark.gpu
+
+CONV_ATOL, CONV_RTOL = 1e-2, 1e-2
+
+
+@pytest.fixture(scope="module")
+def b(cuda_ready):
+    from gemm_conv_epilogues_gb300 import binding
+    return binding
+
+
+def _shape(b, c):
+    return b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad)
+
+
+def _assert_no_device_error(b):
+    rc, word = b.tf_read_device_error()
+    assert rc == b.TF_OK and word == 0, (rc, hex(word))
+
+
+def _conv_check(got, ref):
+    err = np.abs(got - ref)
+    bound = CONV_ATOL + CONV_RTOL * np.abs(ref)
+    bad = err > bound
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outside tolerance; worst {err.max():.4g}"
+
+
+def _run_conv(b, c, d, variant, fused=True):
+    x = dev_u16(d["x"])
+    w = torch.empty((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device="cuda")
+    b.tf_pack_filter_nhwc(dev_u16(d["w_oihw"]), w, c.C_out, c.C_in, c.KH, c.KW)
+    y = torch.full((c.N, c.Ho, c.Wo, c.C_out), 0x7FC0, dtype=torch.int16, device="cuda")  # NaN sentinel
+    if fused:
+        b.tf_conv2d_bn_silu_variant(x, w, dev_f32(d["scale"]), dev_f32(d["bias"]), y, _shape(b, c), variant)
+    else:
+        b.tf_unfused_conv2d(x, w, y, _shape(b, c), variant)
+    torch.cuda.synchronize()
+    return bf16_to_f64(host_u16(y))
+
+
+# ---------------------------------------------------------------- filter pack
+
+@pytest.mark.parametrize("dims", [(16, 8, 3, 3), (256, 256, 1, 1), (64, 24, 7, 7), (5, 3, 2, 4), (1, 1, 1, 1)])
+def test_pack_filter_bit_identical(b, dims):
+    co, ci, kh, kw = dims
+    rng = np.random.default_rng(sum(dims))
+    w = rng.integers(0, 65536, dims).astype(np.uint16)
+    out = torch.zeros((co, kh, kw, ci), dtype=torch.int16, device="cuda")
+    b.tf_pack_filter_nhwc(dev_u16(w), out, co, ci, kh, kw)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_u16(out), oracle.pack_filter(w))
+
+
+def test_pack_filter_full_7x7(b):
+    d = synth.workload_inputs(synth.WORKLOADS["conv7x7_16x64x64x512_to512"])
+    out = torch.zeros((512, 7, 7, 512), dtype=torch.int16, device="cuda")
+    b.tf_pack_filter_nhwc(dev_u16(d["w_oihw"]), out, 512, 512, 7, 7)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_u16(out), oracle.pack_filter(d["w_oihw"]))
+
+
+# ---------------------------------------------------------------- conv, small shapes, full output
+
+CUDA_CORE_SHAPES = [
+    synth.ConvShape(1, 16, 16, 8, 16, 3, 3, (1, 1), (1, 1)),     # the tiny workload
+    synth.ConvShape(2, 9, 7, 16, 20, 3, 3, (1, 1), (1, 1)),      # ragged tiles and channel group
+    synth.ConvShape(1, 11, 13, 24, 5, 5, 3, (2, 1), (2, 1)),     # stride, non-square kernel and pads
+    synth.ConvShape(3, 6, 6, 8, 33, 1, 1, (1, 1), (0, 0)),
+    synth.ConvShape(1, 20, 20, 8, 16, 7, 7, (1, 1), (3, 3)),
+]
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("c", CUDA_CORE_SHAPES, ids=lambda c: f"{c.N}x{c.H}x{c.W}x{c.C_in}-{c.C_out}k{c.KH}{c.KW}s{c.stride[0]}{c.stride[1]}")
+def test_conv_cuda_core_variants(b, c, variant):
+    d = synth.conv_inputs(c, seed=1)
+    got = _run_conv(b, c, d, variant)
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    _conv_check(got, ref)
+
+
+UMMA_SHAPES = [
+    synth.ConvShape(1, 20, 20, 64, 32, 1, 1, (1, 1), (0, 0), ),     # 1x1, one ragged M tile, BN=32
+    synth.ConvShape(2, 15, 17, 128, 256, 1, 1, (1, 1), (0, 0)),     # 1x1, several tiles, ragged tail, BN=256
+    synth.ConvShape(2, 12, 12, 64, 64, 3, 3, (1, 1), (1, 1)),       # im2col 3x3, tiles cross rows and images
+    synth.ConvShape(1, 16, 16, 64, 128, 7, 7, (1, 1), (3, 3)),      # im2col 7x7 pad 3
+    synth.ConvShape(2, 10, 14, 128, 96, 3, 3, (1, 1), (1, 1)),      # non-square image, BN=32, 3 N tiles
+    synth.ConvShape(1, 17, 17, 64, 64, 3, 3, (2, 2), (1, 1)),       # stride 2
+    synth.ConvShape(1, 9, 9, 192, 512, 3, 3, (1, 1), (0, 0)),       # no padding, 2 N tiles of 256
+]
+
+
+@pytest.mark.parametrize("c", UMMA_SHAPES, ids=lambda c: f"{c.N}x{c.H}x{c.W}x{c.C_in}-{c.C_out}k{c.KH}s{c.stride[0]}p{c.pad[0]}")
+def test_conv_umma_small(b, c):
+    d = synth.conv_inputs(c, seed=2, w_dist="normal_fanin")
+    got = _run_conv(b, c, d, b.TF_CONV_UMMA)
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    _conv_check(got, ref)
+    _assert_no_device_error(b)
+
+
+def test_conv_umma_plain_epilogue_is_the_bare_conv(b):
+    c = synth.ConvShape(2, 12, 12, 64, 64, 3, 3, (1, 1), (1, 1))
+    d = synth.conv_inputs(c, seed=3, w_dist="normal_fanin")
+    got = _run_conv(b, c, d, b.TF_CONV_UMMA, fused=False)
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad, oracle.EPI_NONE)
+    _conv_check(got, ref)
+
+
+def test_conv_dispatch_tiny_workload(b):
+    w = synth.WORKLOADS["conv3x3_tiny_1x16x16x8_to16"]
+    c = w.conv
+    d = synth.workload_inputs(w)
+    got = _run_conv(b, c, d, b.TF_CONV_AUTO)
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    _conv_check(got, ref)
+
+
+# ---------------------------------------------------------------- conv, full workloads, sampled
+
+@pytest.mark.parametrize("name,nrand", [("conv1x1_32x56x56x256_to256", 6000), ("conv7x7_16x64x64x512_to512", 1500)])
+def test_conv_full_workload_sampled(b, name, nrand):
+    w = synth.WORKLOADS[name]
+    c = w.conv
+    d = synth.workload_inputs(w)
+    got = _run_conv(b, c, d, b.TF_CONV_AUTO).reshape(-1)
+    pts = conv_sample_points(c.N, c.Ho, c.Wo, c.C_out, nrand, seed=4)
+    ref = oracle.conv2d_bn_silu_points(d["x"], d["w_oihw"], d["scale"], d["bias"], pts, c.stride, c.pad)
+    _conv_check(got[pts], ref)
+    assert np.isfinite(got).all()
+    _assert_no_device_error(b)
+
+
+# ---------------------------------------------------------------- bias + GELU
+
+@pytest.mark.parametrize("rows,cols", [(1, 8), (3, 24), (37, 200), (129, 1032), (8192, 8192)])
+def test_bias_gelu(b, rows, cols):
+    d = synth.bias_gelu_inputs(rows, cols, seed=5)
+    y = torch.empty((rows, cols), dtype=torch.float16, device="cuda")
+    b.tf_bias_gelu(dev_f16(d["x"]), dev_f16(d["bias"]), y, rows, cols)
+    torch.cuda.synchronize()
+    ref = oracle.bias_gelu(d["x"], d["bias"])
+    ulp = f16_ulp_distance(y.cpu().numpy().view(np.uint16), ref)
+    assert ulp.max() <= 2, f"max {ulp.max()} ulp"
+
+
+def test_bias_gelu_negative_tail(b):
+    # s from -10 to 10 on every fp16 value, bias zero: covers the fp16
+    # subnormal outputs of the deep negative tail
+    xs = np.arange(0, 65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    xs = xs[np.isfinite(xs) & (np.abs(xs.astype(np.float32)) <= 10.0)]
+    xs = xs[: (xs.size // 8) * 8].reshape(-1, 8)
+    y = torch.empty(xs.shape, dtype=torch.float16, device="cuda")
+    b.tf_bias_gelu(dev_f16(xs), dev_f16(np.zeros(8, np.float16)), y, xs.shape[0], 8)
+    torch.cuda.synchronize()
+    ref = oracle.bias_gelu(xs, np.zeros(8, np.float16))
+    ulp = f16_ulp_distance(y.cpu().numpy().view(np.uint16), ref)
+    assert ulp.max() <= 2, f"max {ulp.max()} ulp at s={xs.reshape(-1)[ulp.reshape(-1).argmax()]}"
+
+
+# ---------------------------------------------------------------- residual + LayerNorm
+
+@pytest.mark.parametrize("rows,hidden", [(1, 8), (5, 200), (33, 4096), (7, 16384), (16384, 4096)])
+def test_residual_layernorm(b, rows, hidden):
+    d = synth.layernorm_inputs(rows, hidden, seed=6)
+    y = torch.empty((rows, hidden), dtype=torch.float16, device="cuda")
+    b.tf_residual_layernorm(dev_f16(d["act"]), dev_f16(d["res"]), dev_f32(d["gamma"]), dev_f32(d["beta"]), y,
+                            rows, hidden, 1e-5)
+    torch.cuda.synchronize()
+    ref = oracle.residual_layernorm(d["act"], d["res"], d["gamma"], d["beta"], eps=1e-5)
+    err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+    assert err.max() <= 1e-2, err.max()
+
+
+def test_layernorm_constant_row(b):
+    # variance 0: the output is beta exactly (0 * rsqrt(eps) * gamma + beta)
+    rows, hidden = 4, 64
+    act = np.full((rows, hidden), 1.5, np.float16)
+    res = np.full((rows, hidden), -0.25, np.float16)
+    gamma = np.linspace(0.5, 1.5, hidden).astype(np.float32)
+    beta = np.linspace(-1, 1, hidden).astype(np.float32)
+    y = torch.empty((rows, hidden), dtype=torch.float16, device="cuda")
+    b.tf_residual_layernorm(dev_f16(act), dev_f16(res), dev_f32(gamma), dev_f32(beta), y, rows, hidden, 1e-5)
+    torch.cuda.synchronize()
+    ref = oracle.residual_layernorm(act, res, gamma, beta, eps=1e-5)
+    assert np.abs(y.cpu().numpy().astype(np.float64) - ref).max() <= 1e-2
+
+
+# ---------------------------------------------------------------- unfused chains
+
+def test_unfused_conv_chain(b):
+    c = synth.ConvShape(2, 12, 12, 64, 64, 3, 3, (1, 1), (1, 1))
+    d = synth.conv_inputs(c, seed=7, w_dist="normal_fanin")
+    x = dev_u16(d["x"])
+    w = torch.empty((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device="cuda")
+    b.tf_pack_filter_nhwc(dev_u16(d["w_oihw"]), w, c.C_out, c.C_in, c.KH, c.KW)
+    M = c.N * c.Ho * c.Wo
+    t1 = torch.empty((M, c.C_out), dtype=torch.int16, device="cuda")
+    t2 = torch.empty_like(t1)
+    y = torch.empty_like(t1)
+    b.tf_unfused_conv2d(x, w, t1, _shape(b, c), b.TF_CONV_UMMA)
+    b.tf_unfused_bn(t1, dev_f32(d["scale"]), dev_f32(d["bias"]), t2, M, c.C_out)
+    b.tf_unfused_silu(t2, y, M * c.C_out)
+    torch.cuda.synchronize()
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad, oracle.EPI_CHAIN)
+    _conv_check(bf16_to_f64(host_u16(y)).reshape(ref.shape), ref)
+
+
+def test_unfused_gelu_chain(b):
+    rows, cols = 64, 1024
+    d = synth.bias_gelu_inputs(rows, cols, seed=8)
+    t = torch.empty((rows, cols), dtype=torch.float16, device="cuda")
+    y = torch.empty_like(t)
+    b.tf_unfused_bias_add(dev_f16(d["x"]), dev_f16(d["bias"]), t, rows, cols)
+    b.tf_unfused_gelu(t, y, rows * cols)
+    torch.cuda.synchronize()
+    ref = oracle.bias_gelu(d["x"], d["bias"], materialize=True)
+    ulp = f16_ulp_distance(y.cpu().numpy().view(np.uint16), ref)
+    assert ulp.max() <= 2
+
+
+def test_unfused_layernorm_chain(b):
+    rows, hidden = 64, 4096
+    d = synth.layernorm_inputs(rows, hidden, seed=9)
+    s = torch.empty((rows, hidden), dtype=torch.float16, device="cuda")
+    n = torch.empty_like(s)
+    y = torch.empty_like(s)
+    b.tf_unfused_residual_add(dev_f16(d["act"]), dev_f16(d["res"]), s, rows * hidden)
+    b.tf_unfused_layernorm(s, n, rows, hidden, 1e-5)
+    b.tf_unfused_affine(n, dev_f32(d["gamma"]), dev_f32(d["beta"]), y, rows, hidden)
+    torch.cuda.synchronize()
+    ref = oracle.residual_layernorm(d["act"], d["res"], d["gamma"], d["beta"], eps=1e-5, materialize=True)
+    assert np.abs(y.cpu().numpy().astype(np.float64) - ref).max() <= 1e-2
+
+
+# ---------------------------------------------------------------- bounded waits
+
+def test_wait_probe_times_out_and_context_survives(b):
+    _assert_no_device_error(b)
+    b.tf_wait_probe(2_000_000)   # 2 ms on a barrier nothing arrives on
+    rc, word = b.tf_read_device_error()
+    assert rc == b.TF_ERR_TIMEOUT and word == b.TF_DEVERR_PROBE_WAIT
+    _assert_no_device_error(b)   # the word was cleared
+    test_conv_umma_plain_epilogue_is_the_bare_conv(b)   # the context still works
