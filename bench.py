@@ -107,14 +107,15 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def kernel_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel's
-    source has not changed since it was captured (else None)."""
+def kernel_traffic(workload: str):
+    """DRAM bytes (read + write) per launch of the workload's fused kernel from
+    the committed ncu summary, if the kernel's source file has not changed
+    since the capture (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
-        t = json.load(open(path)).get(kernel)
+        t = json.load(open(path)).get(workload)
         if not t:
             return None
         src = os.path.join(ROOT, "gemm_conv_epilogues_gb300", "csrc", t["source"])
@@ -368,6 +369,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-headline", action="store_true")
+    ap.add_argument("--sub-steps", type=int, default=200,
+                    help="timed steps of each secondary workload (the tiny conv runs 10x as many)")
+    ap.add_argument("--profile-workload", default=None,
+                    help="only run W+K fused calls of this workload (for profiler captures)")
+    ap.add_argument("--profile-unfused", action="store_true",
+                    help="with --profile-workload: run the unfused chain instead of the fused call")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -389,6 +396,18 @@ def main():
     barrier(world)
     from gemm_conv_epilogues_gb300 import binding as b
 
+    if args.profile_workload:
+        r = Runner(args.profile_workload, seed=rank)
+        fn = r.unfused if args.profile_unfused else r.fused
+        for i in range(args.warmup + args.steps):
+            fn(i)
+        torch.cuda.synchronize()
+        rc, word = b.tf_read_device_error()
+        if rc != b.TF_OK:
+            raise SystemExit(f"device error word {word:#x}")
+        print(json.dumps({"profile_workload": args.profile_workload, "calls": args.warmup + args.steps}))
+        return
+
     peaks = load_peaks()
     head = Runner(HEADLINE, seed=rank)
     clocks = ClockSampler(local)
@@ -408,7 +427,7 @@ def main():
         "fused": {"ms": ms, "tflops": per_launch_tflops, "gbs": head.alg_bytes / (ms * 1e-3) / 1e9},
         "unfused_chain": {"ms": unf_ms, "launches": 3, "extra_hbm_bytes": head.unfused_extra},
         "roofline": roofline("tensor", per_launch_tflops, peaks["bf16_tflops"], "TFLOP/s",
-                             kernel_traffic("conv_umma_kernel")),
+                             kernel_traffic(HEADLINE)),
     }
     del head
     torch.cuda.empty_cache()
@@ -417,7 +436,7 @@ def main():
         for name in ["conv1x1_32x56x56x256_to256", "bias_gelu_f16_8192x8192",
                      "residual_layernorm_f16_16384x4096", "conv3x3_tiny_1x16x16x8_to16"]:
             r = Runner(name, seed=rank)
-            steps = 200 if r.w.kind != "conv" or r.w.conv.M > 1000 else 2000
+            steps = args.sub_steps if r.w.kind != "conv" or r.w.conv.M > 1000 else 10 * args.sub_steps
             f_ms, _ = time_loop(r.fused, steps, args.warmup, world)
             u_ms, _ = time_loop(r.unfused, steps // 2, args.warmup, world)
             gbs = r.alg_bytes / (f_ms * 1e-3) / 1e9
@@ -427,12 +446,10 @@ def main():
                      "l2": f"{r.nsets} rotating buffer sets"}
             if r.flops:
                 entry["fused"]["tflops"] = r.flops / (f_ms * 1e-3) / 1e12
-            kname = {"conv": "conv_umma_kernel", "bias_gelu": "bias_gelu_kernel",
-                     "layernorm": "layernorm_kernel"}[r.w.kind]
             if name.startswith("conv3x3_tiny"):
                 entry["note"] = "launch-latency bound (0.59 MFLOP); reported as latency"
             else:
-                entry["roofline"] = roofline("hbm", gbs, peaks["hbm_gbs"], "GB/s", kernel_traffic(kname))
+                entry["roofline"] = roofline("hbm", gbs, peaks["hbm_gbs"], "GB/s", kernel_traffic(name))
             workloads[name] = entry
             del r
             torch.cuda.empty_cache()
