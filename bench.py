@@ -107,21 +107,32 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def csrc_fingerprint() -> str:
+    """Hash of every kernel source and header: any change invalidates the
+    DRAM-traffic figures captured before it."""
+    import glob
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "gemm_conv_epilogues_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(d, "*.cu")) + glob.glob(os.path.join(d, "*.h")) +
+                    glob.glob(os.path.join(d, "*.cuh"))):
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(workload: str):
     """DRAM bytes (read + write) per launch of the workload's fused kernel from
-    the committed ncu summary, if the kernel's source file has not changed
-    since the capture (else None)."""
+    the committed ncu summary, if no kernel source has changed since the
+    capture (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
-        t = json.load(open(path)).get(workload)
-        if not t:
+        t = json.load(open(path))
+        if t.get("csrc_sha256_16") != csrc_fingerprint():
             return None
-        src = os.path.join(ROOT, "gemm_conv_epilogues_gb300", "csrc", t["source"])
-        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != t["source_sha256_16"]:
-            return None
-        return float(t["dram_bytes_per_launch"])
+        e = t["workloads"].get(workload)
+        return float(e["dram_bytes_per_launch"]) if e else None
     except Exception:
         return None
 

@@ -9,13 +9,14 @@
 // the padding), which is the TMA_LOAD_IM2COL -> UMMA path that page describes;
 // a 1x1 stride-1 unpadded convolution is a plain matrix, loaded as a 2-D tile.
 //
-// Persistent kernel, one CTA per SM, six warps:
+// Persistent kernel, one CTA per SM, ten warps:
 //   warp 0  TMA producer: a ring of 4 shared-memory stages (A 16 KB + B BN*128 B)
 //   warp 1  TMEM allocator and MMA issuer: tcgen05.mma M=128, N=BN, K=16, fp32
 //           accumulators in TMEM, double-buffered so the epilogue of one tile
 //           overlaps the main loop of the next
-//   warps 2-5 epilogue ("Fusing an Epilogue", "The shape of it"): TMEM ->
-//           registers, v = acc*scale[co] + bias[co], v*sigmoid(v), bf16, store.
+//   warps 2-9 epilogue ("Fusing an Epilogue", "The shape of it"): TMEM ->
+//           registers, v = acc*scale[co] + bias[co], v*sigmoid(v), bf16, then
+//           a swizzled shared-memory box and a TMA store.
 //           The per-channel parameters are read inside the kernel, as in the
 //           page's BatchNorm-epilog listing.
 // Every mbarrier wait is bounded (see ptx::mbar_wait); a role that times out
@@ -34,15 +35,19 @@ constexpr int BM = 128;            // output pixels per tile (UMMA M)
 constexpr int BK = 64;             // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
 constexpr int kStages = 4;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, each taking every other 32-column chunk
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kOutBox = 32;        // epilogue store box: 32 pixels x 32 channels (64 B rows)
+constexpr int kOutBoxBytes = kOutBox * kOutBox * 2;
 
 template <int BN>
 struct Layout {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int BAR_OFFSET = kStages * STAGE_BYTES;
+    static constexpr int OUT_OFFSET = kStages * STAGE_BYTES;                 // 1024-aligned
+    static constexpr int OUT_BYTES = kEpiWarps * 2 * kOutBoxBytes;           // double-buffered per warp
+    static constexpr int BAR_OFFSET = OUT_OFFSET + OUT_BYTES;
     static constexpr int NUM_BARS = 2 * kStages + 5;  // full, empty, tmem full x2, tmem empty x2, drain
     static constexpr int TOTAL = BAR_OFFSET + NUM_BARS * 8 + 16;
     static constexpr int ALLOC = TOTAL + 1024;        // slack to align the base to 1024 B
@@ -64,7 +69,7 @@ struct UmmaParams {
 template <int BN, bool IM2COL>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_umma_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const UmmaParams p)
+                     const __grid_constant__ CUtensorMap tmap_y, const UmmaParams p)
 {
     using L = Layout<BN>;
     extern __shared__ uint8_t smem_raw[];
@@ -91,6 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init_fence();
         ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
+        ptx::prefetch_tensormap(&tmap_y);
     }
     if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, L::TMEM_COLS);
@@ -194,9 +200,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
-        const int row = q * 32 + lane;
-        int local = 0;
+        // Warp w reads TMEM lanes 32*(w%4) .. +31 (one output pixel per lane)
+        // and the 32-column chunks c = h, h+2, ... of the accumulator.  Each
+        // chunk becomes 32 pixels x 32 channels of bf16 in a 64-byte-swizzled
+        // staging box, written to y by one TMA store; two boxes per warp
+        // alternate so conversion overlaps the previous store.
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        uint8_t *stage_out = smem + L::OUT_OFFSET + (warp - 2) * 2 * kOutBoxBytes;
+        int local = 0, nstore = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const int m0 = (tile / p.num_n_tiles) * BM;
@@ -209,45 +221,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-            const int m = m0 + row;
+            const int prow = m0 + q * 32;   // first pixel of this warp's rows
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
-            __nv_bfloat16 *yrow = p.y + (int64_t)m * p.C_out + n0;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = h; c < BN / 32; c += 2) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
-                ptx::tmem_ld_wait();
-                if (m < p.M) {
-                    float v[32];
-                    if (p.epilogue) {
-                        const float4 *sc = reinterpret_cast<const float4 *>(p.scale + n0 + c * 32);
-                        const float4 *bi = reinterpret_cast<const float4 *>(p.bias + n0 + c * 32);
+                float sc[32], bi[32];
+                if (p.epilogue) {
+                    const float4 *s4 = reinterpret_cast<const float4 *>(p.scale + n0 + c * 32);
+                    const float4 *b4 = reinterpret_cast<const float4 *>(p.bias + n0 + c * 32);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 s4 = __ldg(sc + j), b4 = __ldg(bi + j);
-                            v[4 * j + 0] = silu_f32(fmaf(__uint_as_float(r[4 * j + 0]), s4.x, b4.x));
-                            v[4 * j + 1] = silu_f32(fmaf(__uint_as_float(r[4 * j + 1]), s4.y, b4.y));
-                            v[4 * j + 2] = silu_f32(fmaf(__uint_as_float(r[4 * j + 2]), s4.z, b4.z));
-                            v[4 * j + 3] = silu_f32(fmaf(__uint_as_float(r[4 * j + 3]), s4.w, b4.w));
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + c * 32);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint4 o;
-                        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&o);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
-                        dst[j] = o;
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 a4 = __ldg(s4 + j), c4 = __ldg(b4 + j);
+                        sc[4 * j] = a4.x; sc[4 * j + 1] = a4.y; sc[4 * j + 2] = a4.z; sc[4 * j + 3] = a4.w;
+                        bi[4 * j] = c4.x; bi[4 * j + 1] = c4.y; bi[4 * j + 2] = c4.z; bi[4 * j + 3] = c4.w;
                     }
                 }
+                ptx::tmem_ld_wait();
+                uint32_t packed[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float v0 = __uint_as_float(r[2 * j]), v1 = __uint_as_float(r[2 * j + 1]);
+                    if (p.epilogue) {
+                        v0 = silu_f32(fmaf(v0, sc[2 * j], bi[2 * j]));
+                        v1 = silu_f32(fmaf(v1, sc[2 * j + 1], bi[2 * j + 1]));
+                    }
+                    __nv_bfloat162 t = __floats2bfloat162_rn(v0, v1);
+                    packed[j] = *reinterpret_cast<uint32_t *>(&t);
+                }
+                uint8_t *box = stage_out + (nstore & 1) * kOutBoxBytes;
+                // the store issued from this box two chunks ago must have read it
+                if (lane == 0) ptx::bulk_wait_group_read<1>();
+                __syncwarp();
+                // row `lane`, 16-byte chunk j lands at chunk j ^ ((lane >> 1) & 3):
+                // the 64-byte swizzle the store's tensor map expects
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int pj = j ^ ((lane >> 1) & 3);
+                    *reinterpret_cast<uint4 *>(box + lane * 64 + pj * 16) =
+                        make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (prow < p.M) ptx::tma_store_2d(&tmap_y, box, n0 + c * 32, prow);
+                    ptx::bulk_commit_group();
+                }
+                ++nstore;
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&tempty[b]);
         }
+        if (lane == 0) ptx::bulk_wait_group_all();   // stores complete before exit
         if (!ok && lane == 0) atomicOr(p.err, TF_DEVERR_EPILOGUE_WAIT);
     }
 
@@ -312,8 +338,8 @@ bool is_plain_gemm(const tf_conv_shape &s)
 int upper_corner(int in, int out, int stride, int pad) { return (out - 1) * stride - pad - (in - 1); }
 
 template <int BN, bool IM2COL>
-cudaError_t launch_bn(const ConvArgs &a, const CUtensorMap &ta, const CUtensorMap &tb, const UmmaParams &p,
-                      cudaStream_t st)
+cudaError_t launch_bn(const ConvArgs &a, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
+                      const UmmaParams &p, cudaStream_t st)
 {
     using L = Layout<BN>;
     // Per-function, per-device attribute; cheap enough to set on every launch.
@@ -321,19 +347,19 @@ cudaError_t launch_bn(const ConvArgs &a, const CUtensorMap &ta, const CUtensorMa
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
-    conv_umma_kernel<BN, IM2COL><<<grid, kThreads, L::ALLOC, st>>>(ta, tb, p);
+    conv_umma_kernel<BN, IM2COL><<<grid, kThreads, L::ALLOC, st>>>(ta, tb, ty, p);
     return cudaGetLastError();
 }
 
 template <bool IM2COL>
 cudaError_t launch_im(int bn, const ConvArgs &a, const CUtensorMap &ta, const CUtensorMap &tb,
-                      const UmmaParams &p, cudaStream_t st)
+                      const CUtensorMap &ty, const UmmaParams &p, cudaStream_t st)
 {
     switch (bn) {
-    case 256: return launch_bn<256, IM2COL>(a, ta, tb, p, st);
-    case 128: return launch_bn<128, IM2COL>(a, ta, tb, p, st);
-    case 64: return launch_bn<64, IM2COL>(a, ta, tb, p, st);
-    case 32: return launch_bn<32, IM2COL>(a, ta, tb, p, st);
+    case 256: return launch_bn<256, IM2COL>(a, ta, tb, ty, p, st);
+    case 128: return launch_bn<128, IM2COL>(a, ta, tb, ty, p, st);
+    case 64: return launch_bn<64, IM2COL>(a, ta, tb, ty, p, st);
+    case 32: return launch_bn<32, IM2COL>(a, ta, tb, ty, p, st);
     default: return cudaErrorNotSupported;
     }
 }
@@ -367,7 +393,17 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     const int64_t M = (int64_t)s.N * a.Ho * a.Wo;
     const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
 
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ty;
+    {   // y: the NHWC output as a [M][C_out] matrix, stored in 32 x 32 boxes
+        const cuuint64_t dims[2] = {(cuuint64_t)s.C_out, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)s.C_out * 2};
+        const cuuint32_t box[2] = {kOutBox, kOutBox};
+        const cuuint32_t estr[2] = {1, 1};
+        if (tiled(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.y, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     {   // B: packed filters as a [C_out][K] K-major matrix
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)s.C_out};
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
@@ -424,7 +460,7 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     p.num_tiles = (int)((M + BM - 1) / BM) * p.num_n_tiles;
     p.epilogue = a.epilogue;
     if (p.err == nullptr) return cudaErrorInitializationError;
-    return im2col ? launch_im<true>(bn, a, ta, tb, p, st) : launch_im<false>(bn, a, ta, tb, p, st);
+    return im2col ? launch_im<true>(bn, a, ta, tb, ty, p, st) : launch_im<false>(bn, a, ta, tb, ty, p, st);
 }
 
 // ---------------------------------------------------------------- wait probe

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "tf_epilogue.h"
+#include "gelu_poly.h"
 
 namespace tf {
 
@@ -63,9 +64,35 @@ namespace tf {
 // quotient is -0, the correctly rounded fp32 limit.
 __device__ __forceinline__ float silu_f32(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
-// GELU(s) = s * Phi(s) = 0.5 * s * erfc(-s / sqrt(2)), fp32 with CUDA's erfcf;
-// the complement form keeps relative accuracy in the negative tail where
-// 1 + erf(s/sqrt 2) would cancel.
-__device__ __forceinline__ float gelu_f32(float s) { return 0.5f * s * erfcf(-0.70710678118654752f * s); }
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// GELU(s) = s * Phi(s), Phi the standard normal distribution function (the
+// erf definition).  The upper tail Q(t) = 1 - Phi(t) is evaluated as
+// 2^P(t/3 - 1) with P a degree-7 fit of log2 Q on [0, 6] (gelu_poly.h,
+// generated and checked by gen_gelu_poly.py); Phi(s) = 1 - Q(s) for s >= 0
+// and Q(-s) for s < 0, so the negative tail keeps its relative accuracy
+// without the cancellation of 1 + erf.  Beyond |s| = 6 the tail is clamped:
+// |s| * Q(6) is below half the smallest fp16 subnormal.  Cost: 9 FMA-pipe
+// operations and one ex2 per value.
+__device__ __forceinline__ float gelu_f32(float s)
+{
+    const float t = fminf(fabsf(s), TF_GELU_TMAX);
+    const float v = fmaf(t, 1.0f / (TF_GELU_TMAX * 0.5f), -1.0f);
+    float acc = TF_GELU_C7;
+    acc = fmaf(acc, v, TF_GELU_C6);
+    acc = fmaf(acc, v, TF_GELU_C5);
+    acc = fmaf(acc, v, TF_GELU_C4);
+    acc = fmaf(acc, v, TF_GELU_C3);
+    acc = fmaf(acc, v, TF_GELU_C2);
+    acc = fmaf(acc, v, TF_GELU_C1);
+    acc = fmaf(acc, v, TF_GELU_C0);
+    const float q = ex2_approx(acc);
+    return s * (s >= 0.0f ? 1.0f - q : q);
+}
 }  // namespace tf
 #endif
