@@ -242,12 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t packed[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    float v0 = __uint_as_float(r[2 * j]), v1 = __uint_as_float(r[2 * j + 1]);
-                    if (p.epilogue) {
-                        v0 = silu_f32(fmaf(v0, sc[2 * j], bi[2 * j]));
-                        v1 = silu_f32(fmaf(v1, sc[2 * j + 1], bi[2 * j + 1]));
-                    }
-                    __nv_bfloat162 t = __floats2bfloat162_rn(v0, v1);
+                    float2 v = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                    if (p.epilogue)
+                        v = silu_f32x2(ffma2(v, make_float2(sc[2 * j], sc[2 * j + 1]),
+                                             make_float2(bi[2 * j], bi[2 * j + 1])));
+                    __nv_bfloat162 t = __floats2bfloat162_rn(v.x, v.y);
                     packed[j] = *reinterpret_cast<uint32_t *>(&t);
                 }
                 uint8_t *box = stage_out + (nstore & 1) * kOutBoxBytes;

@@ -70,51 +70,69 @@ __device__ __forceinline__ uint4 f_to_b8(const float (&f)[8])
     return v;
 }
 
-// Grid size for a grid-stride kernel over `nvec` 16-byte vectors: enough CTAs
-// to fill every SM several times, never more than the work needs.
-unsigned grid_for(int64_t nvec)
+// Grid size for a grid-stride kernel over `nvec` 16-byte vectors: one wave
+// of resident CTAs, never more than the work needs.
+unsigned grid_for(const void *kernel, int64_t nvec)
 {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
     int64_t per_cta = (int64_t)kThreads * kUnroll;
     int64_t need = (nvec + per_cta - 1) / per_cta;
-    int64_t cap = (int64_t)sm_count() * 8;
+    int64_t cap = (int64_t)sm_count() * per_sm;
     int64_t g = need < cap ? need : cap;
     return (unsigned)(g > 0 ? g : 1);
 }
 
 // ---------------------------------------------------------------- bias + GELU
 
-// y = GELU(x + bias[col]).  cols % 8 == 0, so a 16-byte vector never crosses a
-// row and its eight bias values are bias[col .. col+7].
+// y = GELU(x + bias[col]).  cols % 8 == 0.  A grid-stride loop over 16-byte
+// vectors (8 values) whose stride S is a multiple of the row length in
+// vectors whenever S >= cvec, so each thread's column -- and its bias, kept in
+// registers -- never changes, while the whole grid reads one compact window
+// of the tensor at a time.  Four independent loads are in flight per thread.
 __global__ void __launch_bounds__(kThreads) bias_gelu_kernel(const uint4 *__restrict__ x,
                                                              const uint4 *__restrict__ bias,
                                                              uint4 *__restrict__ y, int64_t nvec,
                                                              int64_t cvec)
 {
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    const int64_t S = (int64_t)gridDim.x * kThreads;
     int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
-        uint4 xv[kUnroll], bv[kUnroll];
+    const bool fixed_col = S % cvec == 0;
+    float b[8];
+    h8_to_f(__ldg(bias + i % cvec), b);
+    for (; i + 3 * S < nvec; i += 4 * S) {
+        uint4 xv[4];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) xv[u] = ld_stream(x + i + u * stride);
+        for (int u = 0; u < 4; ++u) xv[u] = ld_stream(x + i + u * S);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) bv[u] = __ldg(bias + (i + u * stride) % cvec);
+        for (int u = 0; u < 4; ++u) {
+            if (!fixed_col) h8_to_f(__ldg(bias + (i + u * S) % cvec), b);
+            const __half2 *h = reinterpret_cast<const __half2 *>(&xv[u]);
+            uint4 o;
+            __half2 *oh = reinterpret_cast<__half2 *>(&o);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            float a[8], b[8];
-            h8_to_f(xv[u], a);
-            h8_to_f(bv[u], b);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) a[k] = gelu_f32(a[k] + b[k]);
-            st_stream(y + i + u * stride, f_to_h8(a));
+            for (int k = 0; k < 4; ++k) {
+                const float2 sv = fadd2(__half22float2(h[k]), make_float2(b[2 * k], b[2 * k + 1]));
+                const float2 g = gelu_f32x2(sv);
+                oh[k] = __floats2half2_rn(g.x, g.y);
+            }
+            st_stream(y + i + u * S, o);
         }
     }
-    for (; i < nvec; i += stride) {
-        float a[8], b[8];
-        h8_to_f(ld_stream(x + i), a);
-        h8_to_f(__ldg(bias + i % cvec), b);
+    for (; i < nvec; i += S) {
+        if (!fixed_col) h8_to_f(__ldg(bias + i % cvec), b);
+        const uint4 xv = ld_stream(x + i);
+        const __half2 *h = reinterpret_cast<const __half2 *>(&xv);
+        uint4 o;
+        __half2 *oh = reinterpret_cast<__half2 *>(&o);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) a[k] = gelu_f32(a[k] + b[k]);
-        st_stream(y + i, f_to_h8(a));
+        for (int k = 0; k < 4; ++k) {
+            const float2 sv = fadd2(__half22float2(h[k]), make_float2(b[2 * k], b[2 * k + 1]));
+            const float2 g = gelu_f32x2(sv);
+            oh[k] = __floats2half2_rn(g.x, g.y);
+        }
+        st_stream(y + i, o);
     }
 }
 
@@ -175,7 +193,7 @@ cudaError_t launch_chain(const void *a, const void *b, const float *scale, void 
                          int64_t cols, cudaStream_t st)
 {
     const int64_t nvec = n / 8;
-    const unsigned grid = grid_for(nvec);
+    const unsigned grid = grid_for(reinterpret_cast<const void *>(chain_kernel<OP>), nvec);
     chain_kernel<OP><<<grid, kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(a), b, scale,
                                                  reinterpret_cast<uint4 *>(out), nvec, cols / 8);
     return cudaGetLastError();
@@ -207,10 +225,18 @@ __global__ void pack_filter_kernel(const uint16_t *__restrict__ src, uint16_t *_
 cudaError_t launch_bias_gelu(const void *x, const void *bias, void *y, int64_t rows, int64_t cols,
                              cudaStream_t st)
 {
-    const int64_t nvec = rows * cols / 8;
-    bias_gelu_kernel<<<grid_for(nvec), kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(x),
+    const int64_t cvec = cols / 8;
+    const int64_t nvec = rows * cvec;
+    int64_t grid = grid_for(reinterpret_cast<const void *>(bias_gelu_kernel), nvec);
+    // make the stride (grid * threads) a multiple of cvec when it can be, so
+    // every thread keeps one column
+    int64_t a = cvec, bq = kThreads;
+    while (bq) { const int64_t t = a % bq; a = bq; bq = t; }   // gcd(cvec, threads)
+    const int64_t unit = cvec / a;                             // CTAs per whole number of rows
+    if (grid >= unit) grid = grid / unit * unit;
+    bias_gelu_kernel<<<(unsigned)grid, kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(x),
                                                           reinterpret_cast<const uint4 *>(bias),
-                                                          reinterpret_cast<uint4 *>(y), nvec, cols / 8);
+                                                          reinterpret_cast<uint4 *>(y), nvec, cvec);
     return cudaGetLastError();
 }
 

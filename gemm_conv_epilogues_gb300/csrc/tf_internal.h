@@ -59,10 +59,6 @@ cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t st);
 
 #ifdef __CUDACC__
 namespace tf {
-// SiLU(v) = v * sigmoid(v) = v / (1 + e^-v), fp32 ("Fusing an Epilogue",
-// "The shape of it").  For v below about -88 e^-v overflows to +inf and the
-// quotient is -0, the correctly rounded fp32 limit.
-__device__ __forceinline__ float silu_f32(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 __device__ __forceinline__ float ex2_approx(float x)
 {
@@ -76,7 +72,8 @@ __device__ __forceinline__ float ex2_approx(float x)
 // 2^P(t/3 - 1) with P a degree-7 fit of log2 Q on [0, 6] (gelu_poly.h,
 // generated and checked by gen_gelu_poly.py); Phi(s) = 1 - Q(s) for s >= 0
 // and Q(-s) for s < 0, so the negative tail keeps its relative accuracy
-// without the cancellation of 1 + erf.  Beyond |s| = 6 the tail is clamped:
+// without the cancellation of 1 + erf.  With w = s*Q(|s|) that is s - w for
+// s >= 0 and w for s < 0, which is max(s - w, w) since Q <= 1/2.  Beyond |s| = 6 the tail is clamped:
 // |s| * Q(6) is below half the smallest fp16 subnormal.  Cost: 9 FMA-pipe
 // operations and one ex2 per value.
 __device__ __forceinline__ float gelu_f32(float s)
@@ -92,7 +89,105 @@ __device__ __forceinline__ float gelu_f32(float s)
     acc = fmaf(acc, v, TF_GELU_C1);
     acc = fmaf(acc, v, TF_GELU_C0);
     const float q = ex2_approx(acc);
-    return s * (s >= 0.0f ? 1.0f - q : q);
+    const float w = s * q;
+    return fmaxf(s - w, w);
+}
+// ---- packed fp32 pairs (sm_100 family f32x2 instructions): two lanes of
+// work per FMA-pipe issue slot.
+__device__ __forceinline__ unsigned long long pk2(float2 a)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 upk2(unsigned long long r)
+{
+    float2 a;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+    return a;
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
+    return upk2(d);
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk2(a)), "l"(pk2(b)));
+    return upk2(d);
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk2(a)), "l"(pk2(b)));
+    return upk2(d);
+}
+
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b)
+{
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk2(a)), "l"(pk2(b)));
+    return upk2(d);
+}
+
+// gelu_f32 on a pair, same arithmetic: with w = s*Q(|s|), GELU(s) is s - w
+// for s >= 0 and w for s < 0, and in both cases the larger of the two
+// (Q <= 1/2), so the sign test becomes a max.
+__device__ __forceinline__ float2 gelu_f32x2(float2 s)
+{
+    const float2 t = make_float2(fminf(fabsf(s.x), TF_GELU_TMAX), fminf(fabsf(s.y), TF_GELU_TMAX));
+    const float k = 1.0f / (TF_GELU_TMAX * 0.5f);
+    const float2 v = ffma2(t, make_float2(k, k), make_float2(-1.0f, -1.0f));
+    float2 acc = ffma2(make_float2(TF_GELU_C7, TF_GELU_C7), v, make_float2(TF_GELU_C6, TF_GELU_C6));
+    acc = ffma2(acc, v, make_float2(TF_GELU_C5, TF_GELU_C5));
+    acc = ffma2(acc, v, make_float2(TF_GELU_C4, TF_GELU_C4));
+    acc = ffma2(acc, v, make_float2(TF_GELU_C3, TF_GELU_C3));
+    acc = ffma2(acc, v, make_float2(TF_GELU_C2, TF_GELU_C2));
+    acc = ffma2(acc, v, make_float2(TF_GELU_C1, TF_GELU_C1));
+    acc = ffma2(acc, v, make_float2(TF_GELU_C0, TF_GELU_C0));
+    const float2 q = make_float2(ex2_approx(acc.x), ex2_approx(acc.y));
+    const float2 w = fmul2(s, q);
+    const float2 d = fsub2(s, w);
+    return make_float2(fmaxf(d.x, w.x), fmaxf(d.y, w.y));
+}
+// SiLU(v) = v * sigmoid(v) = v / (1 + 2^(-v*log2 e)) ("Fusing an Epilogue",
+// "The shape of it").  One ex2 per value; the reciprocal of d = 1 + 2^x runs
+// on the FMA pipe instead of the special-function unit: an integer-subtraction
+// seed (subtracting the float's bit pattern from a constant approximates
+// 1/d to within 5.1% because the bit pattern is a piecewise-linear log2),
+// then two Newton-Raphson steps r <- r + r*(1 - d*r), each squaring the
+// relative error (5.1e-2 -> 2.6e-3 -> 6.5e-6).  x is clamped to 64 so d stays
+// a normal float; for v < -44 the result is within 1e-17 of zero.
+// The seed works on -d: bits(1/d) ~ 0xFEF311C3 - bits(-d) (mod 2^32).
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kRcpSeed = 0xFEF311C3u;
+
+__device__ __forceinline__ float silu_f32(float v)
+{
+    const float u = ex2_approx(fminf(-kLog2e * v, 64.0f));
+    const float nd = -1.0f - u;                                   // -(1 + u)
+    float r = __uint_as_float(kRcpSeed - __float_as_uint(nd));    // ~ 1/(1 + u)
+    r = fmaf(r, fmaf(nd, r, 1.0f), r);
+    r = fmaf(r, fmaf(nd, r, 1.0f), r);
+    return v * r;
+}
+
+__device__ __forceinline__ float2 silu_f32x2(float2 v)
+{
+    const float2 x = fmul2(v, make_float2(-kLog2e, -kLog2e));
+    const float2 u = make_float2(ex2_approx(fminf(x.x, 64.0f)), ex2_approx(fminf(x.y, 64.0f)));
+    const float2 nd = ffma2(u, make_float2(-1.0f, -1.0f), make_float2(-1.0f, -1.0f));
+    float2 r = make_float2(__uint_as_float(kRcpSeed - __float_as_uint(nd.x)),
+                           __uint_as_float(kRcpSeed - __float_as_uint(nd.y)));
+    r = ffma2(r, ffma2(nd, r, make_float2(1.0f, 1.0f)), r);
+    r = ffma2(r, ffma2(nd, r, make_float2(1.0f, 1.0f)), r);
+    return fmul2(v, r);
 }
 }  // namespace tf
 #endif
