@@ -153,13 +153,21 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """Largest value over the ranks (the slowest rank's time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_throughput(units_per_rank: float, ms_slowest: float, world: int, scale: float = 1e12) -> float:
+    """Weak scaling: every rank processes `units_per_rank`; the job's rate is
+    all ranks' units over the slowest rank's time (per second, / scale)."""
+    return units_per_rank * world / (ms_slowest * 1e-3) / scale
 
 
 # ---------------------------------------------------------------- workloads
@@ -204,12 +212,14 @@ class Runner:
             self.t2 = torch.empty_like(self.t1)
             self.host_x = torch.from_numpy(d["x"].view(np.int16).copy()).pin_memory()
             self.host_y = torch.empty((c.M, c.C_out), dtype=torch.int16).pin_memory()
-        elif w.kind == "bias_gelu":
+        elif w.kind in ("bias_gelu", "bias_gelu_rowsum"):
             rows, cols = w.rows, w.cols
             self.flops = 0
             n = rows * cols
-            self.alg_bytes = 2 * n + 2 * n + 2 * cols
-            self.unfused_extra = 4 * n
+            self.alg_bytes = 2 * n + 2 * n + 2 * cols + (4 * rows if w.kind == "bias_gelu_rowsum" else 0)
+            # split paths: the x + bias intermediate (write + read), or the re-read of y by the reduction
+            self.unfused_extra = 4 * n if w.kind == "bias_gelu" else 2 * n
+            self.rowsum = torch.empty((rows,), dtype=torch.float32, device=dev)
             self.h2d, self.d2h = 2 * n, 2 * n
             per_set = 4 * n
             nsets = max(1, int(np.ceil(2 * L2_BYTES / per_set)) + 1)
@@ -245,6 +255,8 @@ class Runner:
             b.tf_conv2d_bn_silu(s["x"], self.wt, self.scale, self.bias, s["y"], self.shape)
         elif w.kind == "bias_gelu":
             b.tf_bias_gelu(s["x"], self.bias, s["y"], w.rows, w.cols)
+        elif w.kind == "bias_gelu_rowsum":
+            b.tf_bias_gelu_rowsum(s["x"], self.bias, s["y"], self.rowsum, w.rows, w.cols)
         else:
             b.tf_residual_layernorm(s["a"], s["r"], self.gamma, self.beta, s["y"], w.rows, w.cols, w.eps)
         return 1
@@ -260,6 +272,10 @@ class Runner:
         if w.kind == "bias_gelu":
             b.tf_unfused_bias_add(s["x"], self.bias, self.t, w.rows, w.cols)
             b.tf_unfused_gelu(self.t, s["y"], w.rows * w.cols)
+            return 2
+        if w.kind == "bias_gelu_rowsum":
+            b.tf_bias_gelu(s["x"], self.bias, s["y"], w.rows, w.cols)
+            b.tf_unfused_rowsum(s["y"], self.rowsum, w.rows, w.cols)
             return 2
         b.tf_unfused_residual_add(s["a"], s["r"], self.s, w.rows * w.cols)
         b.tf_unfused_layernorm(self.s, self.n, w.rows, w.cols, w.eps)
@@ -423,11 +439,10 @@ def main():
     head = Runner(HEADLINE, seed=rank)
     clocks = ClockSampler(local)
     ms, launches = time_loop(head.fused, args.steps, args.warmup, world, clocks)
-    total_flops = head.flops * world
-    value = total_flops / (ms * 1e-3) / 1e12
+    value = whole_job_throughput(head.flops, ms, world)
     per_launch_tflops = head.flops / (ms * 1e-3) / 1e12
     e2e_ms, _ = time_loop(head.e2e, max(5, args.steps // 20), args.warmup, world)
-    e2e_val = total_flops / (e2e_ms * 1e-3) / 1e12
+    e2e_val = whole_job_throughput(head.flops, e2e_ms, world)
     rc, word = b.tf_read_device_error()
     if rc != b.TF_OK:
         raise SystemExit(f"device error word {word:#x} after the timed region")
@@ -444,7 +459,7 @@ def main():
     torch.cuda.empty_cache()
 
     if not args.only_headline:
-        for name in ["conv1x1_32x56x56x256_to256", "bias_gelu_f16_8192x8192",
+        for name in ["conv1x1_32x56x56x256_to256", "bias_gelu_f16_8192x8192", "bias_gelu_rowsum_f16_8192x8192",
                      "residual_layernorm_f16_16384x4096", "conv3x3_tiny_1x16x16x8_to16"]:
             r = Runner(name, seed=rank)
             steps = args.sub_steps if r.w.kind != "conv" or r.w.conv.M > 1000 else 10 * args.sub_steps

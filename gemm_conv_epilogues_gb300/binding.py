@@ -44,6 +44,8 @@ _SIGS = {
     "tf_conv2d_bn_silu_variant": ([_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(tf_conv_shape), _i, _vp], _i),
     "tf_conv2d_bn_silu_select": ([ctypes.POINTER(tf_conv_shape)], _i),
     "tf_bias_gelu": ([_vp, _vp, _vp, _i64, _i64, _vp], _i),
+    "tf_bias_gelu_rowsum": ([_vp, _vp, _vp, _vp, _i64, _i64, _vp], _i),
+    "tf_unfused_rowsum": ([_vp, _vp, _i64, _i64, _vp], _i),
     "tf_residual_layernorm": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f, _vp], _i),
     "tf_unfused_conv2d": ([_vp, _vp, _vp, ctypes.POINTER(tf_conv_shape), _i, _vp], _i),
     "tf_unfused_bn": ([_vp, _vp, _vp, _vp, _i64, _i64, _vp], _i),
@@ -125,6 +127,16 @@ def tf_conv2d_bn_silu_select(shape) -> int:
 def tf_bias_gelu(x, bias, y, rows, cols, stream=None, check=True):
     return _check(_lib.tf_bias_gelu(_ptr(x), _ptr(bias), _ptr(y), rows, cols, _stream(stream)),
                   "tf_bias_gelu", check)
+
+
+def tf_bias_gelu_rowsum(x, bias, y, rowsum, rows, cols, stream=None, check=True):
+    return _check(_lib.tf_bias_gelu_rowsum(_ptr(x), _ptr(bias), _ptr(y), _ptr(rowsum), rows, cols, _stream(stream)),
+                  "tf_bias_gelu_rowsum", check)
+
+
+def tf_unfused_rowsum(y, rowsum, rows, cols, stream=None, check=True):
+    return _check(_lib.tf_unfused_rowsum(_ptr(y), _ptr(rowsum), rows, cols, _stream(stream)),
+                  "tf_unfused_rowsum", check)
 
 
 def tf_residual_layernorm(act, res, gamma, beta, y, rows, hidden, eps, stream=None, check=True):

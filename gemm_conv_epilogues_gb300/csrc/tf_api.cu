@@ -94,15 +94,24 @@ int check_conv_shape(const tf_conv_shape *s, int *Ho, int *Wo)
     return TF_OK;
 }
 
-// Kernel choice by shape.  Thresholds: see the measured table in the bench
-// (a flop count below which the tensor-core pipeline's fixed cost of one
-// persistent wave does not pay, and a channel count at which the tiled
-// kernel's 16-channel groups stop wasting lanes).
+// Kernel choice by shape ("Fusing an Epilogue", "Three kernels for one
+// operation").  Thresholds measured on GB300 by
+// gemm_conv_epilogues_gb300/dispatch_sweep.py (GPU time of CUDA-graph
+// replays over 108 shapes):
+//  - the tensor-core kernel wins wherever it can run, except on tiny
+//    reductions (K = C_in*KH*KW <= 64 and under 10 MFLOP), where its fixed
+//    cost (~3.7 us for one persistent wave) loses to the direct kernel;
+//  - among the CUDA-core kernels the tiled one wins from 16384 output pixels
+//    up, or with few input channels (<= 16) once there are at least ~2M
+//    output-channel-taps (M * C_out * KH * KW) to share each staged halo.
 int select_variant(const tf_conv_shape &s, int Ho, int Wo)
 {
-    const double flops = 2.0 * s.N * Ho * Wo * (double)s.C_out * s.KH * s.KW * s.C_in;
-    if (conv_umma_supports(s, Ho, Wo) && s.C_out >= 32 && flops >= 64.0e6) return TF_CONV_UMMA;
-    if (s.C_out > 16 && (int64_t)s.N * Ho * Wo >= 256) return TF_CONV_TILED;
+    const int64_t M = (int64_t)s.N * Ho * Wo;
+    const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
+    const double flops = 2.0 * (double)M * s.C_out * (double)K;
+    if (conv_umma_supports(s, Ho, Wo) && !(K <= 64 && flops < 10.0e6)) return TF_CONV_UMMA;
+    const double taps = (double)M * s.C_out * s.KH * s.KW;
+    if (M >= 16384 || (s.C_in <= 16 && taps >= 2.0e6)) return TF_CONV_TILED;
     return TF_CONV_DIRECT;
 }
 
@@ -177,6 +186,22 @@ int tf_bias_gelu(const void *x, const void *bias, void *y, int64_t rows, int64_t
     if (!x || !bias || !y || bad_rows_cols(rows, cols)) return TF_ERR_INVALID_ARG;
     if (cols % 8 != 0 || !aligned16(x) || !aligned16(bias) || !aligned16(y)) return TF_ERR_UNSUPPORTED;
     return from_cuda(launch_bias_gelu(x, bias, y, rows, cols, (cudaStream_t)stream));
+}
+
+int tf_bias_gelu_rowsum(const void *x, const void *bias, void *y, float *rowsum, int64_t rows, int64_t cols,
+                        tf_stream_t stream)
+{
+    if (!x || !bias || !y || !rowsum || bad_rows_cols(rows, cols)) return TF_ERR_INVALID_ARG;
+    if (cols % 8 != 0 || cols > 16384 || !aligned16(x) || !aligned16(bias) || !aligned16(y))
+        return TF_ERR_UNSUPPORTED;
+    return from_cuda(launch_bias_gelu_rowsum(x, bias, y, rowsum, rows, cols, (cudaStream_t)stream));
+}
+
+int tf_unfused_rowsum(const void *y, float *rowsum, int64_t rows, int64_t cols, tf_stream_t stream)
+{
+    if (!y || !rowsum || bad_rows_cols(rows, cols)) return TF_ERR_INVALID_ARG;
+    if (cols % 8 != 0 || cols > 16384 || !aligned16(y)) return TF_ERR_UNSUPPORTED;
+    return from_cuda(launch_unfused_rowsum(y, rowsum, rows, cols, (cudaStream_t)stream));
 }
 
 int tf_residual_layernorm(const void *act, const void *res, const float *gamma, const float *beta, void *y,

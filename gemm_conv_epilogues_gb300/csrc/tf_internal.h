@@ -53,6 +53,9 @@ cudaError_t launch_unfused_layernorm(const void *s, void *nrm, int64_t rows, int
                                      float eps, cudaStream_t st);
 cudaError_t launch_unfused_affine(const void *nrm, const float *gamma, const float *beta, void *y,
                                   int64_t rows, int64_t hidden, cudaStream_t st);
+cudaError_t launch_bias_gelu_rowsum(const void *x, const void *bias, void *y, float *rowsum, int64_t rows,
+                                    int64_t cols, cudaStream_t st);
+cudaError_t launch_unfused_rowsum(const void *y, float *rowsum, int64_t rows, int64_t cols, cudaStream_t st);
 cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t st);
 
 }  // namespace tf

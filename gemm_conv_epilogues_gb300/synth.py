@@ -113,7 +113,7 @@ def layernorm_inputs(rows: int, hidden: int, seed: int = 0) -> dict:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "conv", "bias_gelu" or "layernorm"
+    kind: str                 # "conv", "bias_gelu", "bias_gelu_rowsum" or "layernorm"
     conv: ConvShape | None = None
     w_dist: str = "uniform"
     rows: int = 0
@@ -128,6 +128,7 @@ WORKLOADS = {
         Workload("conv3x3_tiny_1x16x16x8_to16", "conv",
                  ConvShape(1, 16, 16, 8, 16, 3, 3, (1, 1), (1, 1)), "uniform"),
         Workload("bias_gelu_f16_8192x8192", "bias_gelu", rows=8192, cols=8192),
+        Workload("bias_gelu_rowsum_f16_8192x8192", "bias_gelu_rowsum", rows=8192, cols=8192),
         Workload("residual_layernorm_f16_16384x4096", "layernorm", rows=16384, cols=4096, eps=1e-5),
         Workload("conv1x1_32x56x56x256_to256", "conv",
                  ConvShape(32, 56, 56, 256, 256, 1, 1, (1, 1), (0, 0)), "normal_fanin"),
@@ -140,7 +141,7 @@ WORKLOADS = {
 def workload_inputs(w: Workload, seed: int = 0) -> dict:
     if w.kind == "conv":
         return conv_inputs(w.conv, seed, w.w_dist)
-    if w.kind == "bias_gelu":
+    if w.kind in ("bias_gelu", "bias_gelu_rowsum"):
         return bias_gelu_inputs(w.rows, w.cols, seed)
     if w.kind == "layernorm":
         return layernorm_inputs(w.rows, w.cols, seed)

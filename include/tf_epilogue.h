@@ -129,6 +129,17 @@ int tf_conv2d_bn_silu_select(const tf_conv_shape *shape);
 int tf_bias_gelu(const void *x, const void *bias, void *y, int64_t rows, int64_t cols,
                  tf_stream_t stream);
 
+/* Bias + GELU + per-row sum in one pass.  "Costs and benefits of kernel
+ * fusion", "Compare fused and split bias-activation-reduction paths": apply
+ * bias, GELU and a per-row reduction without writing the GELU result before
+ * the reduction reads it.
+ *   x, y : fp16 [rows][cols];  bias : fp16 [cols];  rowsum : fp32 [rows]
+ * y[i][j] = GELU(x[i][j] + bias[j]) as in tf_bias_gelu; rowsum[i] = sum over
+ * j of the fp32 GELU values (before y is rounded to fp16), accumulated in
+ * fp32.  Requires cols % 8 == 0, cols <= 16384, 16-byte aligned x, bias, y. */
+int tf_bias_gelu_rowsum(const void *x, const void *bias, void *y, float *rowsum, int64_t rows,
+                        int64_t cols, tf_stream_t stream);
+
 /* ---------------------------------------------------------------- residual + LN */
 
 /* y = LayerNorm(act + res) * gamma + beta, one HBM pass.  "Costs and benefits
@@ -164,6 +175,10 @@ int tf_unfused_silu(const void *t2, void *y, int64_t n, tf_stream_t stream);
 /* t[i][j] = x[i][j] + bias[j]; fp16, cols % 8 == 0. */
 int tf_unfused_bias_add(const void *x, const void *bias, void *t, int64_t rows, int64_t cols,
                         tf_stream_t stream);
+/* rowsum[i] = sum over j of y[i][j] (fp16 in, fp32 sum): the reduction of
+ * the split bias-activation-reduction path, run after tf_bias_gelu has
+ * written y.  cols % 8 == 0, cols <= 16384. */
+int tf_unfused_rowsum(const void *y, float *rowsum, int64_t rows, int64_t cols, tf_stream_t stream);
 /* y = GELU(t); fp16, n % 8 == 0. */
 int tf_unfused_gelu(const void *t, void *y, int64_t n, tf_stream_t stream);
 /* s = act + res; fp16, n % 8 == 0. */

@@ -77,6 +77,9 @@ def test_host_validation_rejects_before_launch(native_lib):
     assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 8, -1.0, 0, check=False) == S
     assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 20, 1e-5, 0, check=False) == U
     assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 32768, 1e-5, 0, check=False) == U
+    assert b.tf_bias_gelu_rowsum(p16, p16, p16, None, 4, 8, 0, check=False) == S
+    assert b.tf_bias_gelu_rowsum(p16, p16, p16, p16, 4, 32768, 0, check=False) == U
+    assert b.tf_unfused_rowsum(p16, p16, 4, 12, 0, check=False) == U
     assert b.tf_pack_filter_nhwc(None, p16, 4, 4, 3, 3, 0, check=False) == S
     assert b.tf_pack_filter_nhwc(p16, p16, 0, 4, 3, 3, 0, check=False) == S
     assert b.tf_unfused_bn(p16, p16, p16, p16, 4, 12, 0, check=False) == U
@@ -95,5 +98,11 @@ def test_dispatch_selects_by_shape(native_lib):
     assert sel(w["conv1x1_32x56x56x256_to256"].conv) == b.TF_CONV_UMMA
     assert sel(w["conv7x7_16x64x64x512_to512"].conv) == b.TF_CONV_UMMA
     # shapes the tensor-core kernel cannot take go to the CUDA-core kernels
-    assert sel(synth.ConvShape(8, 32, 32, 24, 48, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
+    assert sel(synth.ConvShape(16, 32, 32, 24, 48, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
+    assert sel(synth.ConvShape(4, 32, 32, 8, 64, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
+    assert sel(synth.ConvShape(4, 32, 32, 8, 32, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_DIRECT
+    assert sel(synth.ConvShape(4, 32, 32, 256, 16, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_DIRECT
+    # tiny reductions stay on the direct kernel even when the tensor-core one could run
+    assert sel(synth.ConvShape(1, 16, 16, 64, 64, 1, 1)) == b.TF_CONV_DIRECT
+    assert sel(synth.ConvShape(1, 16, 16, 256, 64, 1, 1)) == b.TF_CONV_UMMA
     assert b.tf_conv2d_bn_silu_select(b.conv_shape(1, 2, 2, 8, 16, 5, 5)) == -b.TF_ERR_INVALID_ARG

@@ -176,6 +176,44 @@ def test_bias_gelu_negative_tail(b):
     assert ulp.max() <= 2, f"max {ulp.max()} ulp at s={xs.reshape(-1)[ulp.reshape(-1).argmax()]}"
 
 
+# ---------------------------------------------------------------- bias + GELU + row sum
+
+# Row-sum tolerance: each term carries the GELU evaluation error (~1e-5
+# relative) and, on the split path, the fp16 rounding of y (<= 2^-12
+# relative); fp32 accumulation over <= 16384 terms in a shallow tree adds
+# ~30 * 2^-24 relative.  Bound: 1e-3 * sum_j |y_j| + 1e-3, four times the
+# worst case.
+def _rowsum_check(rs_gpu, y_ref):
+    bound = 1e-3 * np.abs(y_ref).sum(axis=1) + 1e-3
+    err = np.abs(rs_gpu.astype(np.float64) - y_ref.sum(axis=1))
+    assert np.all(err <= bound), f"worst row error {err.max():.4g} (bound {bound[err.argmax()]:.4g})"
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 8), (3, 200), (37, 1032), (300, 16384), (8192, 8192)])
+def test_bias_gelu_rowsum_fused(b, rows, cols):
+    d = synth.bias_gelu_inputs(rows, cols, seed=10)
+    y = torch.empty((rows, cols), dtype=torch.float16, device="cuda")
+    rs = torch.full((rows,), float("nan"), dtype=torch.float32, device="cuda")
+    b.tf_bias_gelu_rowsum(dev_f16(d["x"]), dev_f16(d["bias"]), y, rs, rows, cols)
+    torch.cuda.synchronize()
+    ref_y, ref_rs = oracle.bias_gelu_rowsum(d["x"], d["bias"])
+    assert f16_ulp_distance(y.cpu().numpy().view(np.uint16), ref_y).max() <= 2
+    _rowsum_check(rs.cpu().numpy(), ref_y)
+    _assert_no_device_error(b)
+
+
+@pytest.mark.parametrize("rows,cols", [(3, 200), (8192, 8192)])
+def test_bias_gelu_rowsum_split(b, rows, cols):
+    d = synth.bias_gelu_inputs(rows, cols, seed=11)
+    y = torch.empty((rows, cols), dtype=torch.float16, device="cuda")
+    rs = torch.empty((rows,), dtype=torch.float32, device="cuda")
+    b.tf_bias_gelu(dev_f16(d["x"]), dev_f16(d["bias"]), y, rows, cols)
+    b.tf_unfused_rowsum(y, rs, rows, cols)
+    torch.cuda.synchronize()
+    ref_y, _ = oracle.bias_gelu_rowsum(d["x"], d["bias"])
+    _rowsum_check(rs.cpu().numpy(), ref_y)
+
+
 # ---------------------------------------------------------------- residual + LayerNorm
 
 @pytest.mark.parametrize("rows,hidden", [(1, 8), (5, 200), (33, 4096), (7, 16384), (16384, 4096)])
