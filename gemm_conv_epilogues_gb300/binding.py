@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libtf_epilogue.so")
 
 TF_OK, TF_ERR_INVALID_ARG, TF_ERR_UNSUPPORTED, TF_ERR_CUDA, TF_ERR_TIMEOUT = 0, 1, 2, 3, 4
 TF_CONV_AUTO, TF_CONV_DIRECT, TF_CONV_TILED, TF_CONV_UMMA = -1, 0, 1, 2
+TF_LN_AUTO, TF_LN_WARP, TF_LN_CTA, TF_LN_CLUSTER = -1, 0, 1, 2
 TF_DEVERR_PRODUCER_WAIT, TF_DEVERR_MMA_WAIT, TF_DEVERR_EPILOGUE_WAIT = 0x1, 0x2, 0x4
 TF_DEVERR_DRAIN_WAIT, TF_DEVERR_PROBE_WAIT = 0x8, 0x10
 
@@ -47,6 +48,8 @@ _SIGS = {
     "tf_bias_gelu_rowsum": ([_vp, _vp, _vp, _vp, _i64, _i64, _vp], _i),
     "tf_unfused_rowsum": ([_vp, _vp, _i64, _i64, _vp], _i),
     "tf_residual_layernorm": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f, _vp], _i),
+    "tf_residual_layernorm_variant": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f, _i, _vp], _i),
+    "tf_residual_layernorm_select": ([_i64], _i),
     "tf_unfused_conv2d": ([_vp, _vp, _vp, ctypes.POINTER(tf_conv_shape), _i, _vp], _i),
     "tf_unfused_bn": ([_vp, _vp, _vp, _vp, _i64, _i64, _vp], _i),
     "tf_unfused_silu": ([_vp, _vp, _i64, _vp], _i),
@@ -142,6 +145,16 @@ def tf_unfused_rowsum(y, rowsum, rows, cols, stream=None, check=True):
 def tf_residual_layernorm(act, res, gamma, beta, y, rows, hidden, eps, stream=None, check=True):
     return _check(_lib.tf_residual_layernorm(_ptr(act), _ptr(res), _ptr(gamma), _ptr(beta), _ptr(y), rows,
                                              hidden, float(eps), _stream(stream)), "tf_residual_layernorm", check)
+
+
+def tf_residual_layernorm_variant(act, res, gamma, beta, y, rows, hidden, eps, variant, stream=None, check=True):
+    return _check(_lib.tf_residual_layernorm_variant(_ptr(act), _ptr(res), _ptr(gamma), _ptr(beta), _ptr(y), rows,
+                                                     hidden, float(eps), int(variant), _stream(stream)),
+                  "tf_residual_layernorm_variant", check)
+
+
+def tf_residual_layernorm_select(hidden) -> int:
+    return _lib.tf_residual_layernorm_select(int(hidden))
 
 
 def tf_unfused_conv2d(x, w_ohwi, t1, shape, variant=TF_CONV_AUTO, stream=None, check=True):

@@ -200,6 +200,246 @@ __global__ void __launch_bounds__(1024) layernorm_kernel(const __half *__restric
     }
 }
 
+// ---------------------------------------------------------------- one warp per row
+
+// Narrow rows (hidden <= 1024): a warp owns a row, so both reductions are
+// warp shuffles with no block barrier.  Lane l holds the 16-byte vectors
+// l, l+32, ... (NV of them) of act and res; a CTA of 8 warps works on 8
+// rows at once and the grid strides over the rest.
+template <int NV, bool RESIDUAL, bool AFFINE>
+__global__ void __launch_bounds__(256) layernorm_warp_kernel(const __half *__restrict__ a,
+                                                             const __half *__restrict__ b,
+                                                             const float *__restrict__ gamma,
+                                                             const float *__restrict__ beta,
+                                                             __half *__restrict__ y, int64_t rows, int hidden,
+                                                             float eps)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int nvec = hidden >> 3;
+    const float inv_h = 1.0f / (float)hidden;
+    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < rows; row += nwarps) {
+        uint4 av[NV], bv[NV];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int v = lane + 32 * k;
+            av[k] = make_uint4(0, 0, 0, 0);
+            bv[k] = make_uint4(0, 0, 0, 0);
+            if (v < nvec) {
+                av[k] = ld_stream(a + row * hidden + 8 * v);
+                if (RESIDUAL) bv[k] = ld_stream(b + row * hidden + 8 * v);
+            }
+        }
+        float s[NV][8];
+        float sum = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const __half2 *ah = reinterpret_cast<const __half2 *>(&av[k]);
+            const __half2 *bh = reinterpret_cast<const __half2 *>(&bv[k]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float2 t = __half22float2(ah[j]);
+                if (RESIDUAL) {
+                    const float2 u = __half22float2(bh[j]);
+                    t.x += u.x;
+                    t.y += u.y;
+                }
+                s[k][2 * j] = t.x;
+                s[k][2 * j + 1] = t.y;
+                sum += t.x + t.y;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float mean = sum * inv_h;
+        float sq = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            if (lane + 32 * k < nvec) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float d = s[k][j] - mean;
+                    sq = fmaf(d, d, sq);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        const float rstd = rsqrtf(sq * inv_h + eps);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int v = lane + 32 * k;
+            if (v >= nvec) continue;
+            float g[8], bb[8];
+            if (AFFINE) {
+                const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gamma + 8 * v));
+                const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gamma + 8 * v + 4));
+                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + 8 * v));
+                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + 8 * v + 4));
+                g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w; g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+                bb[0] = b0.x; bb[1] = b0.y; bb[2] = b0.z; bb[3] = b0.w; bb[4] = b1.x; bb[5] = b1.y; bb[6] = b1.z; bb[7] = b1.w;
+            }
+            uint4 out;
+            __half2 *oh = reinterpret_cast<__half2 *>(&out);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float o0 = (s[k][2 * j] - mean) * rstd, o1 = (s[k][2 * j + 1] - mean) * rstd;
+                oh[j] = AFFINE ? __floats2half2_rn(fmaf(o0, g[2 * j], bb[2 * j]), fmaf(o1, g[2 * j + 1], bb[2 * j + 1]))
+                               : __floats2half2_rn(o0, o1);
+            }
+            st_stream(y + row * hidden + 8 * v, out);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- a cluster per row
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster; orders shared-memory writes before
+// the barrier with reads of them (local or remote) after it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Reads a float from the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_dsmem(const float *local, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ptx::smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float cta_sum(float v, float *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = lane < nwarps ? red[lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
+
+// Wide rows (hidden > 16384): a thread-block cluster owns a row; CTA r of the
+// cluster holds the slice [r*slice, (r+1)*slice) in registers (2 vectors per
+// thread).  Each reduction is a CTA sum followed by an exchange of the
+// per-CTA partials through distributed shared memory, so the row is still
+// read from HBM exactly once ("a hidden width large enough to require a
+// different row-reduction strategy").
+template <bool RESIDUAL, bool AFFINE>
+__global__ void __launch_bounds__(1024) layernorm_cluster_kernel(const __half *__restrict__ a,
+                                                                 const __half *__restrict__ b,
+                                                                 const float *__restrict__ gamma,
+                                                                 const float *__restrict__ beta,
+                                                                 __half *__restrict__ y, int hidden, int slice,
+                                                                 float eps)
+{
+    constexpr int NV = 2;
+    __shared__ float red[32];
+    __shared__ float part[2];
+    const uint32_t rank = cluster_ctarank(), nranks = cluster_nctarank();
+    const int64_t row = blockIdx.x / nranks;
+    const int c0 = (int)rank * slice;                    // first column of this CTA's slice
+    const int nvec = (min(hidden - c0, slice)) >> 3;     // vectors in the slice
+    const __half *ar = a + row * hidden + c0;
+    const __half *br = RESIDUAL ? b + row * hidden + c0 : nullptr;
+
+    float s[NV][8];
+    float sum = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int v = threadIdx.x + k * blockDim.x;
+        uint4 av = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
+        if (v < nvec) {
+            av = ld_stream(ar + 8 * v);
+            if (RESIDUAL) bv = ld_stream(br + 8 * v);
+        }
+        const __half2 *ah = reinterpret_cast<const __half2 *>(&av);
+        const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float2 t = __half22float2(ah[j]);
+            if (RESIDUAL) {
+                const float2 u = __half22float2(bh[j]);
+                t.x += u.x;
+                t.y += u.y;
+            }
+            s[k][2 * j] = t.x;
+            s[k][2 * j + 1] = t.y;
+            sum += t.x + t.y;
+        }
+    }
+    const float inv_h = 1.0f / (float)hidden;
+    float total = cta_sum(sum, red);
+    if (threadIdx.x == 0) part[0] = total;
+    cluster_sync();
+    total = 0.0f;
+    for (uint32_t r = 0; r < nranks; ++r) total += ld_dsmem(&part[0], r);
+    const float mean = total * inv_h;
+    float sq = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        if (threadIdx.x + k * blockDim.x < nvec) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float d = s[k][j] - mean;
+                sq = fmaf(d, d, sq);
+            }
+        }
+    }
+    float sqt = cta_sum(sq, red);
+    if (threadIdx.x == 0) part[1] = sqt;
+    cluster_sync();
+    sqt = 0.0f;
+    for (uint32_t r = 0; r < nranks; ++r) sqt += ld_dsmem(&part[1], r);
+    cluster_sync();   // no CTA leaves while another may still read its `part`
+    const float rstd = rsqrtf(sqt * inv_h + eps);
+    __half *yr = y + row * hidden + c0;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int v = threadIdx.x + k * blockDim.x;
+        if (v >= nvec) continue;
+        float g[8], bb[8];
+        if (AFFINE) {
+            const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gamma + c0 + 8 * v));
+            const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gamma + c0 + 8 * v + 4));
+            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + c0 + 8 * v));
+            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + c0 + 8 * v + 4));
+            g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w; g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+            bb[0] = b0.x; bb[1] = b0.y; bb[2] = b0.z; bb[3] = b0.w; bb[4] = b1.x; bb[5] = b1.y; bb[6] = b1.z; bb[7] = b1.w;
+        }
+        uint4 out;
+        __half2 *oh = reinterpret_cast<__half2 *>(&out);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float o0 = (s[k][2 * j] - mean) * rstd, o1 = (s[k][2 * j + 1] - mean) * rstd;
+            oh[j] = AFFINE ? __floats2half2_rn(fmaf(o0, g[2 * j], bb[2 * j]), fmaf(o1, g[2 * j + 1], bb[2 * j + 1]))
+                           : __floats2half2_rn(o0, o1);
+        }
+        st_stream(yr + 8 * v, out);
+    }
+}
+
 // y[i][j] = nrm[i][j] * gamma[j] + beta[j] (the unfused chain's last kernel).
 __global__ void __launch_bounds__(256) affine_kernel(const uint4 *__restrict__ nrm,
                                                      const float *__restrict__ gamma,
@@ -233,10 +473,10 @@ int threads_for(int64_t hidden, int nv)
 }
 
 template <bool RESIDUAL, bool AFFINE>
-cudaError_t launch_ln(const void *a, const void *b, const float *gamma, const float *beta, void *y,
-                      int64_t rows, int64_t hidden, float eps, cudaStream_t st)
+cudaError_t launch_ln_cta(const void *a, const void *b, const float *gamma, const float *beta, void *y,
+                          int64_t rows, int64_t hidden, float eps, cudaStream_t st)
 {
-    if (hidden > 2048 * 8) return cudaErrorNotSupported;
+    if (hidden > kCtaMaxHidden) return cudaErrorNotSupported;
     uint32_t *err = device_error_word();
     if (!err) return cudaErrorInitializationError;
     const int threads = threads_for(hidden, 2);
@@ -245,35 +485,106 @@ cudaError_t launch_ln(const void *a, const void *b, const float *gamma, const fl
     int stages = (int)((96 * 1024) / stage_bytes);
     stages = stages < 2 ? 2 : (stages > 4 ? 4 : stages);
     const size_t smem = (size_t)stages * stage_bytes + 8 * (size_t)stages;
-    // CTAs per SM: limited by shared memory (~220 KB usable) and 2048 threads.
-    int per_sm = (int)((220 * 1024) / (smem + 1024));
-    if (per_sm > 2048 / threads) per_sm = 2048 / threads;
-    if (per_sm > 8) per_sm = 8;
-    if (per_sm < 1) per_sm = 1;
-    int64_t grid = (int64_t)sm_count() * per_sm;
-    if (grid > rows) grid = rows;
     auto kern = layernorm_kernel<2, RESIDUAL, AFFINE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    int64_t grid = (int64_t)sm_count() * per_sm;
+    if (grid > rows) grid = rows;
     kern<<<(unsigned)grid, threads, smem, st>>>(reinterpret_cast<const __half *>(a), reinterpret_cast<const __half *>(b),
                                                 gamma, beta, reinterpret_cast<__half *>(y), rows, (int)hidden, eps,
                                                 stages, err, wait_limit_ns());
     return cudaGetLastError();
 }
 
+template <bool RESIDUAL, bool AFFINE>
+cudaError_t launch_ln_warp(const void *a, const void *b, const float *gamma, const float *beta, void *y,
+                           int64_t rows, int64_t hidden, float eps, cudaStream_t st)
+{
+    if (hidden > kWarpMaxHidden) return cudaErrorNotSupported;
+    const int nvec = (int)(hidden / 8);
+    auto pick = [&](auto kern) -> cudaError_t {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)
+            per_sm = 1;
+        int64_t grid = (int64_t)sm_count() * per_sm;
+        const int64_t need = (rows + 7) / 8;
+        if (grid > need) grid = need;
+        kern<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const __half *>(a), reinterpret_cast<const __half *>(b),
+                                             gamma, beta, reinterpret_cast<__half *>(y), rows, (int)hidden, eps);
+        return cudaGetLastError();
+    };
+    if (nvec <= 32) return pick(layernorm_warp_kernel<1, RESIDUAL, AFFINE>);
+    if (nvec <= 64) return pick(layernorm_warp_kernel<2, RESIDUAL, AFFINE>);
+    return pick(layernorm_warp_kernel<4, RESIDUAL, AFFINE>);
+}
+
+template <bool RESIDUAL, bool AFFINE>
+cudaError_t launch_ln_cluster(const void *a, const void *b, const float *gamma, const float *beta, void *y,
+                              int64_t rows, int64_t hidden, float eps, cudaStream_t st)
+{
+    if (hidden > kClusterMaxHidden) return cudaErrorNotSupported;
+    // Fewest CTAs per row (at most 8, the portable cluster size) with at
+    // most 1024 threads x 16 values each; the slice is a multiple of 8.
+    int csize = 1;
+    while ((int64_t)csize * 1024 * 16 < hidden) ++csize;
+    if (csize < 2) csize = 2;
+    const int64_t slice = ((hidden + csize - 1) / csize + 7) / 8 * 8;
+    const int threads = threads_for(slice, 2);
+    if (rows * csize > 0x7fffffff) return cudaErrorNotSupported;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows * csize));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, layernorm_cluster_kernel<RESIDUAL, AFFINE>, reinterpret_cast<const __half *>(a),
+                              reinterpret_cast<const __half *>(b), gamma, beta, reinterpret_cast<__half *>(y),
+                              (int)hidden, (int)slice, eps);
+}
+
+template <bool RESIDUAL, bool AFFINE>
+cudaError_t launch_ln(const void *a, const void *b, const float *gamma, const float *beta, void *y,
+                      int64_t rows, int64_t hidden, float eps, int variant, cudaStream_t st)
+{
+    if (variant == TF_LN_AUTO) variant = layernorm_select(hidden);
+    switch (variant) {
+    case TF_LN_WARP: return launch_ln_warp<RESIDUAL, AFFINE>(a, b, gamma, beta, y, rows, hidden, eps, st);
+    case TF_LN_CTA: return launch_ln_cta<RESIDUAL, AFFINE>(a, b, gamma, beta, y, rows, hidden, eps, st);
+    case TF_LN_CLUSTER: return launch_ln_cluster<RESIDUAL, AFFINE>(a, b, gamma, beta, y, rows, hidden, eps, st);
+    default: return cudaErrorNotSupported;
+    }
+}
+
 }  // namespace
+
+int layernorm_select(int64_t hidden)
+{
+    if (hidden <= kWarpBoundary) return TF_LN_WARP;
+    if (hidden <= kCtaMaxHidden) return TF_LN_CTA;
+    if (hidden <= kClusterMaxHidden) return TF_LN_CLUSTER;
+    return -TF_ERR_UNSUPPORTED;
+}
 
 cudaError_t launch_residual_layernorm(const void *act, const void *res, const float *gamma,
                                       const float *beta, void *y, int64_t rows, int64_t hidden,
-                                      float eps, cudaStream_t st)
+                                      float eps, int variant, cudaStream_t st)
 {
-    return launch_ln<true, true>(act, res, gamma, beta, y, rows, hidden, eps, st);
+    return launch_ln<true, true>(act, res, gamma, beta, y, rows, hidden, eps, variant, st);
 }
 
 cudaError_t launch_unfused_layernorm(const void *s, void *nrm, int64_t rows, int64_t hidden, float eps,
                                      cudaStream_t st)
 {
-    return launch_ln<false, false>(s, nullptr, nullptr, nullptr, nrm, rows, hidden, eps, st);
+    return launch_ln<false, false>(s, nullptr, nullptr, nullptr, nrm, rows, hidden, eps, TF_LN_AUTO, st);
 }
 
 cudaError_t launch_unfused_affine(const void *nrm, const float *gamma, const float *beta, void *y,

@@ -204,15 +204,30 @@ int tf_unfused_rowsum(const void *y, float *rowsum, int64_t rows, int64_t cols, 
     return from_cuda(launch_unfused_rowsum(y, rowsum, rows, cols, (cudaStream_t)stream));
 }
 
-int tf_residual_layernorm(const void *act, const void *res, const float *gamma, const float *beta, void *y,
-                          int64_t rows, int64_t hidden, float eps, tf_stream_t stream)
+int tf_residual_layernorm_variant(const void *act, const void *res, const float *gamma, const float *beta,
+                                  void *y, int64_t rows, int64_t hidden, float eps, int variant, tf_stream_t stream)
 {
     if (!act || !res || !gamma || !beta || !y || bad_rows_cols(rows, hidden) || !(eps >= 0.0f))
         return TF_ERR_INVALID_ARG;
-    if (hidden % 8 != 0 || hidden > 16384 || rows > 0x7fffffff) return TF_ERR_UNSUPPORTED;
+    if (variant < TF_LN_AUTO || variant > TF_LN_CLUSTER) return TF_ERR_INVALID_ARG;
+    if (hidden % 8 != 0 || hidden > kClusterMaxHidden || rows > 0x7fffffff) return TF_ERR_UNSUPPORTED;
     if (!aligned16(act) || !aligned16(res) || !aligned16(gamma) || !aligned16(beta) || !aligned16(y))
         return TF_ERR_UNSUPPORTED;
-    return from_cuda(launch_residual_layernorm(act, res, gamma, beta, y, rows, hidden, eps, (cudaStream_t)stream));
+    return from_cuda(
+        launch_residual_layernorm(act, res, gamma, beta, y, rows, hidden, eps, variant, (cudaStream_t)stream));
+}
+
+int tf_residual_layernorm(const void *act, const void *res, const float *gamma, const float *beta, void *y,
+                          int64_t rows, int64_t hidden, float eps, tf_stream_t stream)
+{
+    return tf_residual_layernorm_variant(act, res, gamma, beta, y, rows, hidden, eps, TF_LN_AUTO, stream);
+}
+
+int tf_residual_layernorm_select(int64_t hidden)
+{
+    if (hidden <= 0) return -TF_ERR_INVALID_ARG;
+    if (hidden % 8 != 0) return -TF_ERR_UNSUPPORTED;
+    return layernorm_select(hidden);
 }
 
 int tf_unfused_conv2d(const void *x, const void *w_ohwi, void *t1, const tf_conv_shape *shape, int variant,
@@ -261,7 +276,7 @@ int tf_unfused_residual_add(const void *act, const void *res, void *s, int64_t n
 int tf_unfused_layernorm(const void *s, void *nrm, int64_t rows, int64_t hidden, float eps, tf_stream_t stream)
 {
     if (!s || !nrm || bad_rows_cols(rows, hidden) || !(eps >= 0.0f)) return TF_ERR_INVALID_ARG;
-    if (hidden % 8 != 0 || hidden > 16384 || rows > 0x7fffffff || !aligned16(s) || !aligned16(nrm))
+    if (hidden % 8 != 0 || hidden > kClusterMaxHidden || rows > 0x7fffffff || !aligned16(s) || !aligned16(nrm))
         return TF_ERR_UNSUPPORTED;
     return from_cuda(launch_unfused_layernorm(s, nrm, rows, hidden, eps, (cudaStream_t)stream));
 }

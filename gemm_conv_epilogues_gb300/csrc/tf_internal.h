@@ -38,9 +38,17 @@ cudaError_t launch_pack_filter(const void *w_oihw, void *w_ohwi, int C_out, int 
                                cudaStream_t st);
 cudaError_t launch_bias_gelu(const void *x, const void *bias, void *y, int64_t rows, int64_t cols,
                              cudaStream_t st);
+// Row-reduction strategy boundaries of the LayerNorm kernels (hidden widths).
+constexpr int64_t kWarpMaxHidden = 1024;      // warp per row: up to 4 vectors per lane
+constexpr int64_t kCtaMaxHidden = 16384;      // CTA per row: up to 1024 threads x 16 values
+constexpr int64_t kClusterMaxHidden = 131072; // cluster of <= 8 CTAs per row
+// Measured on GB300 (gemm_conv_epilogues_gb300/ln_sweep.py): one warp per row
+// is faster up to this width, one CTA per row above it.
+constexpr int64_t kWarpBoundary = 1024;
+int layernorm_select(int64_t hidden);
 cudaError_t launch_residual_layernorm(const void *act, const void *res, const float *gamma,
                                       const float *beta, void *y, int64_t rows, int64_t hidden,
-                                      float eps, cudaStream_t st);
+                                      float eps, int variant, cudaStream_t st);
 cudaError_t launch_unfused_bn(const void *t1, const float *scale, const float *bias, void *t2,
                               int64_t M, int64_t C, cudaStream_t st);
 cudaError_t launch_unfused_silu(const void *t2, void *y, int64_t n, cudaStream_t st);

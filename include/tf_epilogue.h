@@ -65,6 +65,16 @@ typedef enum {
     TF_CONV_UMMA = 2     /* implicit GEMM: TMA im2col -> tcgen05.mma -> TMEM -> fused epilogue */
 } tf_conv_variant;
 
+/* Row-reduction strategies of the LayerNorm kernels (see
+ * tf_residual_layernorm_variant). */
+typedef enum {
+    TF_LN_AUTO = -1,    /* by hidden width */
+    TF_LN_WARP = 0,     /* one warp per row, shuffle reductions (hidden <= 1024) */
+    TF_LN_CTA = 1,      /* one CTA per row, rows streamed through a bulk-copy ring (hidden <= 16384) */
+    TF_LN_CLUSTER = 2   /* a cluster of <= 8 CTAs per row, partials exchanged through
+                           distributed shared memory (16384 < hidden <= 131072) */
+} tf_ln_variant;
+
 /* Human-readable name of a status code (static storage). */
 const char *tf_status_string(int status);
 
@@ -148,11 +158,25 @@ int tf_bias_gelu_rowsum(const void *x, const void *bias, void *y, float *rowsum,
  * normalise, apply scale and bias, write the final output.
  *   act, res, y : fp16 [rows][hidden];  gamma, beta : fp32 [hidden]
  * mean and biased variance of s = act + res per row, computed in fp32 from
- * registers in two passes (s is never written); y = (s - mean) /
- * sqrt(var + eps) * gamma + beta.  Requires hidden % 8 == 0,
- * hidden <= 16384, 16-byte aligned pointers, eps >= 0. */
+ * registers in two passes (sum, then squared deviations; s is never
+ * written); y = (s - mean) / sqrt(var + eps) * gamma + beta.  Requires
+ * hidden % 8 == 0, hidden <= 131072, 16-byte aligned pointers, eps >= 0.
+ * The row-reduction strategy is chosen by hidden width
+ * (tf_residual_layernorm_select). */
 int tf_residual_layernorm(const void *act, const void *res, const float *gamma, const float *beta,
                           void *y, int64_t rows, int64_t hidden, float eps, tf_stream_t stream);
+
+/* Same with the strategy forced (TF_LN_*); TF_ERR_UNSUPPORTED when the width
+ * is outside the strategy's range.  "Costs and benefits of kernel fusion",
+ * worked example: test a hidden width large enough to require a different
+ * row-reduction strategy, with an explicit dispatch boundary. */
+int tf_residual_layernorm_variant(const void *act, const void *res, const float *gamma,
+                                  const float *beta, void *y, int64_t rows, int64_t hidden,
+                                  float eps, int variant, tf_stream_t stream);
+
+/* The strategy tf_residual_layernorm uses for this width (host only), or a
+ * negative tf_status value when no strategy takes it. */
+int tf_residual_layernorm_select(int64_t hidden);
 
 /* ---------------------------------------------------------------- unfused chains */
 
@@ -184,7 +208,8 @@ int tf_unfused_gelu(const void *t, void *y, int64_t n, tf_stream_t stream);
 /* s = act + res; fp16, n % 8 == 0. */
 int tf_unfused_residual_add(const void *act, const void *res, void *s, int64_t n,
                             tf_stream_t stream);
-/* nrm = (s - mean)/sqrt(var + eps) per row, no affine; fp16 in and out. */
+/* nrm = (s - mean)/sqrt(var + eps) per row, no affine; fp16 in and out
+ * (hidden <= 131072, same strategies as tf_residual_layernorm). */
 int tf_unfused_layernorm(const void *s, void *nrm, int64_t rows, int64_t hidden, float eps,
                          tf_stream_t stream);
 /* y[i][j] = nrm[i][j]*gamma[j] + beta[j]; fp16 in and out, fp32 gamma/beta. */

@@ -76,7 +76,13 @@ def test_host_validation_rejects_before_launch(native_lib):
     assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 0, 1e-5, 0, check=False) == S
     assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 8, -1.0, 0, check=False) == S
     assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 20, 1e-5, 0, check=False) == U
-    assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 32768, 1e-5, 0, check=False) == U
+    assert b.tf_residual_layernorm(p16, p16, p16, p16, p16, 4, 262144, 1e-5, 0, check=False) == U
+    assert b.tf_residual_layernorm_variant(p16, p16, p16, p16, p16, 4, 64, 1e-5, 5, 0, check=False) == S
+    assert b.tf_residual_layernorm_select(512) == b.TF_LN_WARP
+    assert b.tf_residual_layernorm_select(4096) == b.TF_LN_CTA
+    assert b.tf_residual_layernorm_select(65536) == b.TF_LN_CLUSTER
+    assert b.tf_residual_layernorm_select(262144) == -b.TF_ERR_UNSUPPORTED
+    assert b.tf_residual_layernorm_select(100) == -b.TF_ERR_UNSUPPORTED
     assert b.tf_bias_gelu_rowsum(p16, p16, p16, None, 4, 8, 0, check=False) == S
     assert b.tf_bias_gelu_rowsum(p16, p16, p16, p16, 4, 32768, 0, check=False) == U
     assert b.tf_unfused_rowsum(p16, p16, 4, 12, 0, check=False) == U

@@ -228,6 +228,35 @@ def test_residual_layernorm(b, rows, hidden):
     assert err.max() <= 1e-2, err.max()
 
 
+@pytest.mark.parametrize("variant,rows,hidden", [
+    (0, 5, 8), (0, 37, 200), (0, 64, 1024), (0, 3, 1000),
+    (1, 5, 8), (1, 9, 8200), (1, 4, 16384),
+    (2, 3, 16392), (2, 5, 40000), (2, 2, 131072),
+])
+def test_layernorm_each_strategy(b, variant, rows, hidden):
+    d = synth.layernorm_inputs(rows, hidden, seed=12)
+    y = torch.empty((rows, hidden), dtype=torch.float16, device="cuda")
+    b.tf_residual_layernorm_variant(dev_f16(d["act"]), dev_f16(d["res"]), dev_f32(d["gamma"]), dev_f32(d["beta"]),
+                                    y, rows, hidden, 1e-5, variant)
+    torch.cuda.synchronize()
+    ref = oracle.residual_layernorm(d["act"], d["res"], d["gamma"], d["beta"], eps=1e-5)
+    err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+    assert err.max() <= 1e-2, err.max()
+    _assert_no_device_error(b)
+
+
+def test_layernorm_wide_rows_dispatch(b):
+    rows, hidden = 6, 65536
+    assert b.tf_residual_layernorm_select(hidden) == b.TF_LN_CLUSTER
+    d = synth.layernorm_inputs(rows, hidden, seed=13)
+    y = torch.empty((rows, hidden), dtype=torch.float16, device="cuda")
+    b.tf_residual_layernorm(dev_f16(d["act"]), dev_f16(d["res"]), dev_f32(d["gamma"]), dev_f32(d["beta"]), y,
+                            rows, hidden, 1e-5)
+    torch.cuda.synchronize()
+    ref = oracle.residual_layernorm(d["act"], d["res"], d["gamma"], d["beta"], eps=1e-5)
+    assert np.abs(y.cpu().numpy().astype(np.float64) - ref).max() <= 1e-2
+
+
 def test_layernorm_constant_row(b):
     # variance 0: the output is beta exactly (0 * rsqrt(eps) * gamma + beta)
     rows, hidden = 4, 64
