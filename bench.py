@@ -296,6 +296,59 @@ class Runner:
         return k
 
 
+class PairRunner:
+    """Producer -> consumer convs with the activation between them either in
+    the producer's epilogue (fused) or as standalone kernels (BN, then SiLU)
+    between a plain producer conv and the consumer."""
+
+    def __init__(self, seed: int):
+        import torch
+        from gemm_conv_epilogues_gb300 import binding as b, synth
+        self.b = b
+        p, c = synth.PAIR_PRODUCER, synth.PAIR_CONSUMER
+        self.p, self.c = p, c
+        d = synth.producer_consumer_inputs(p, c, seed)
+        dev = "cuda"
+        up16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16).copy()).to(dev)
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+        self.w1 = torch.empty((p.C_out, p.KH, p.KW, p.C_in), dtype=torch.int16, device=dev)
+        self.w2 = torch.empty((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device=dev)
+        b.tf_pack_filter_nhwc(up16(d["w1_oihw"]), self.w1, p.C_out, p.C_in, p.KH, p.KW)
+        b.tf_pack_filter_nhwc(up16(d["w2_oihw"]), self.w2, c.C_out, c.C_in, c.KH, c.KW)
+        self.s1, self.b1, self.s2, self.b2 = up(d["scale1"]), up(d["bias1"]), up(d["scale2"]), up(d["bias2"])
+        self.sh1 = b.conv_shape(p.N, p.H, p.W, p.C_in, p.C_out, p.KH, p.KW, p.stride, p.pad)
+        self.sh2 = b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad)
+        x_bytes = p.N * p.H * p.W * p.C_in * 2
+        u_bytes = p.M * p.C_out * 2
+        nsets = max(1, int(np.ceil(2 * L2_BYTES / (x_bytes + 2 * u_bytes))) + 1)
+        x0 = up16(d["x"])
+        self.sets = [{"x": x0.clone(), "u": torch.empty((p.M, p.C_out), dtype=torch.int16, device=dev),
+                      "y": torch.empty((c.M, c.C_out), dtype=torch.int16, device=dev)} for _ in range(nsets)]
+        self.t = torch.empty((p.M, p.C_out), dtype=torch.int16, device=dev)
+        self.t2 = torch.empty_like(self.t)
+        self.nsets = nsets
+        self.u_elems = p.M * p.C_out
+
+    def fused(self, i):
+        b, s = self.b, self.sets[i % self.nsets]
+        b.tf_conv2d_bn_silu(s["x"], self.w1, self.s1, self.b1, s["u"], self.sh1)
+        b.tf_conv2d_bn_silu(s["u"], self.w2, self.s2, self.b2, s["y"], self.sh2)
+        return 2
+
+    def standalone(self, i):
+        b, s = self.b, self.sets[i % self.nsets]
+        b.tf_unfused_conv2d(s["x"], self.w1, self.t, self.sh1)
+        self.activation(i)
+        b.tf_conv2d_bn_silu(s["u"], self.w2, self.s2, self.b2, s["y"], self.sh2)
+        return 4
+
+    def activation(self, i):
+        b, s = self.b, self.sets[i % self.nsets]
+        b.tf_unfused_bn(self.t, self.s1, self.b1, self.t2, self.p.M, self.p.C_out)
+        b.tf_unfused_silu(self.t2, s["u"], self.u_elems)
+        return 2
+
+
 def time_loop(fn, steps: int, warmup: int, world: int, clocks=None):
     """Times exactly `steps` calls of fn(i) with CUDA events on the current
     stream, bracketed by a barrier and a device synchronise on both sides;
@@ -479,6 +532,22 @@ def main():
             workloads[name] = entry
             del r
             torch.cuda.empty_cache()
+
+        # the activation between two convs: in the producer's epilogue, or standalone
+        pr = PairRunner(seed=rank)
+        steps = max(10, args.sub_steps // 4)
+        f_ms, _ = time_loop(pr.fused, steps, args.warmup, world)
+        s_ms, _ = time_loop(pr.standalone, steps, args.warmup, world)
+        a_ms, _ = time_loop(pr.activation, steps, args.warmup, world)
+        workloads["producer_consumer_1x1_256to128_then_7x7_128to128"] = {
+            "fused_pipeline_ms": f_ms, "standalone_activation_pipeline_ms": s_ms,
+            "standalone_activation_kernels_ms": a_ms,
+            "standalone_activation_share_of_busy": a_ms / s_ms,
+            "note": "producer 1x1 conv -> BN+SiLU -> consumer 7x7 conv on 16x64x64; fused puts BN+SiLU in the "
+                    "producer's epilogue (write cardinality), standalone runs a plain producer conv then BN and "
+                    "SiLU kernels"}
+        del pr
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -44,6 +44,8 @@ _SIGS = {
     "tf_conv2d_bn_silu": ([_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(tf_conv_shape), _vp], _i),
     "tf_conv2d_bn_silu_variant": ([_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(tf_conv_shape), _i, _vp], _i),
     "tf_conv2d_bn_silu_select": ([ctypes.POINTER(tf_conv_shape)], _i),
+    "tf_conv2d_bn_silu_workspace_size": ([ctypes.POINTER(tf_conv_shape)], _i64),
+    "tf_conv2d_bn_silu_ws": ([_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(tf_conv_shape), _vp, _i64, _vp], _i),
     "tf_bias_gelu": ([_vp, _vp, _vp, _i64, _i64, _vp], _i),
     "tf_bias_gelu_rowsum": ([_vp, _vp, _vp, _vp, _i64, _i64, _vp], _i),
     "tf_unfused_rowsum": ([_vp, _vp, _i64, _i64, _vp], _i),
@@ -125,6 +127,16 @@ def tf_conv2d_bn_silu_variant(x, w_ohwi, scale, bias, y, shape, variant, stream=
 
 def tf_conv2d_bn_silu_select(shape) -> int:
     return _lib.tf_conv2d_bn_silu_select(ctypes.byref(shape))
+
+
+def tf_conv2d_bn_silu_workspace_size(shape) -> int:
+    return int(_lib.tf_conv2d_bn_silu_workspace_size(ctypes.byref(shape)))
+
+
+def tf_conv2d_bn_silu_ws(x, w_ohwi, scale, bias, y, shape, workspace, workspace_bytes, stream=None, check=True):
+    return _check(_lib.tf_conv2d_bn_silu_ws(_ptr(x), _ptr(w_ohwi), _ptr(scale), _ptr(bias), _ptr(y),
+                                            ctypes.byref(shape), _ptr(workspace), int(workspace_bytes),
+                                            _stream(stream)), "tf_conv2d_bn_silu_ws", check)
 
 
 def tf_bias_gelu(x, bias, y, rows, cols, stream=None, check=True):

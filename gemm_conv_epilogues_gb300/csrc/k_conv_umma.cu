@@ -63,7 +63,9 @@ struct UmmaParams {
     int M, C_out, KW, HoWo, Wo;
     int stride_h, stride_w, pad_h, pad_w;
     int num_kb, cblocks, num_n_tiles, num_tiles;
-    int epilogue;
+    int epilogue;            // 0: plain bf16 store, 1: BN + SiLU, 2: fp32 split-K partial to ws
+    int splits, kb_per_split, num_work;   // work item = (tile, K split), split fastest
+    float *ws;               // split-K partials [splits][M][C_out] (epilogue 2 only)
 };
 
 template <int BN, bool IM2COL>
@@ -114,14 +116,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued = 0, last_phase = 0;  // per-stage bit masks
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            for (int work = blockIdx.x; ok && work < p.num_work; work += gridDim.x) {
+                const int tile = work / p.splits;
+                const int kb_begin = (work - tile * p.splits) * p.kb_per_split;
+                const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
                 const int m0 = (tile / p.num_n_tiles) * BM;
                 const int n0 = (tile % p.num_n_tiles) * BN;
                 const int img = m0 / p.HoWo;
                 const int rem = m0 - img * p.HoWo;
                 const int oh = rem / p.Wo, ow = rem - (rem / p.Wo) * p.Wo;
                 const int w_base = ow * p.stride_w - p.pad_w, h_base = oh * p.stride_h - p.pad_h;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
                         ok = false;
                         break;
@@ -162,7 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+            for (int work = blockIdx.x; ok && work < p.num_work; work += gridDim.x, ++local) {
+                const int kb_begin = (work % p.splits) * p.kb_per_split;
+                const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
                 const int b = local & 1;
                 const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
                 if (!ptx::mbar_wait(&tempty[b], acc_phase ^ 1u, p.wait_ns)) {
@@ -171,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!ptx::mbar_wait(&full[stage], phase, p.wait_ns)) {
                         ok = false;
                         break;
@@ -183,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         ptx::umma_bf16(d_tmem, ptx::sw128_kmajor_desc(a_addr + k * UMMA_K * 2),
                                        ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2), idesc,
-                                       (kb > 0 || k > 0) ? 1u : 0u);
+                                       (kb > kb_begin || k > 0) ? 1u : 0u);
                     }
                     ptx::umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
                     if (++stage == kStages) {
@@ -210,7 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *stage_out = smem + L::OUT_OFFSET + (warp - 2) * 2 * kOutBoxBytes;
         int local = 0, nstore = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+        for (int work = blockIdx.x; work < p.num_work; work += gridDim.x, ++local) {
+            const int tile = work / p.splits;
+            const int split = work - tile * p.splits;
             const int m0 = (tile / p.num_n_tiles) * BM;
             const int n0 = (tile % p.num_n_tiles) * BN;
             const int b = local & 1;
@@ -227,6 +236,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = h; c < BN / 32; c += 2) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                if (p.epilogue == 2) {
+                    // split-K partial: this lane's row, 32 fp32 channels, 128 contiguous bytes
+                    ptx::tmem_ld_wait();
+                    const int m = prow + lane;
+                    if (m < p.M) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)split * p.M + m) * p.C_out + n0 + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    }
+                    continue;
+                }
                 float sc[32], bi[32];
                 if (p.epilogue) {
                     const float4 *s4 = reinterpret_cast<const float4 *>(p.scale + n0 + c * 32);
@@ -345,7 +367,7 @@ cudaError_t launch_bn(const ConvArgs &a, const CUtensorMap &ta, const CUtensorMa
     cudaError_t e = cudaFuncSetAttribute(conv_umma_kernel<BN, IM2COL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
+    const int grid = p.num_work < sm_count() ? p.num_work : sm_count();
     conv_umma_kernel<BN, IM2COL><<<grid, kThreads, L::ALLOC, st>>>(ta, tb, ty, p);
     return cudaGetLastError();
 }
@@ -458,8 +480,89 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     p.num_n_tiles = s.C_out / bn;
     p.num_tiles = (int)((M + BM - 1) / BM) * p.num_n_tiles;
     p.epilogue = a.epilogue;
+    p.splits = 1;
+    p.kb_per_split = p.num_kb;
+    p.ws = nullptr;
+    if (a.splits > 1) {
+        if (!a.ws) return cudaErrorInvalidValue;
+        p.kb_per_split = (p.num_kb + a.splits - 1) / a.splits;
+        p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;   // no empty split
+        p.epilogue = 2;
+        p.ws = a.ws;
+    }
+    p.num_work = p.num_tiles * p.splits;
     if (p.err == nullptr) return cudaErrorInitializationError;
     return im2col ? launch_im<true>(bn, a, ta, tb, ty, p, st) : launch_im<false>(bn, a, ta, tb, ty, p, st);
+}
+
+// ---------------------------------------------------------------- split K
+
+int conv_umma_splits(const tf_conv_shape &s, int Ho, int Wo)
+{
+    const int bn = pick_bn(s.C_out);
+    if (bn == 0) return 1;
+    const int64_t M = (int64_t)s.N * Ho * Wo;
+    const int64_t tiles = (M + BM - 1) / BM * (s.C_out / bn);
+    const int64_t num_kb = (int64_t)s.KH * s.KW * s.C_in / BK;
+    const int sms = sm_count();
+    if (tiles * 2 > sms) return 1;          // at least half the SMs busy already
+    if (num_kb < 16) return 1;              // short K loops: the extra reduction costs more than it saves
+    int64_t S = sms / tiles;
+    if (S > num_kb / 4) S = num_kb / 4;     // at least 4 K blocks per split
+    if (S < 2) return 1;
+    const int64_t kbps = (num_kb + S - 1) / S;
+    return (int)((num_kb + kbps - 1) / kbps);
+}
+
+namespace {
+// y = epilogue(sum over splits of the fp32 partials), 8 channels per thread.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ ws, int splits, int64_t MC,
+                                                            int C_out, const float *__restrict__ scale,
+                                                            const float *__restrict__ bias,
+                                                            __nv_bfloat16 *__restrict__ y, int epilogue)
+{
+    const int64_t nvec = MC / 8;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        float v[8];
+        const float4 *src = reinterpret_cast<const float4 *>(ws) + 2 * i;
+        float4 a = __ldcs(src), b = __ldcs(src + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        for (int sidx = 1; sidx < splits; ++sidx) {
+            const float4 *q = reinterpret_cast<const float4 *>(ws + sidx * MC) + 2 * i;
+            a = __ldcs(q);
+            b = __ldcs(q + 1);
+            v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w; v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+        }
+        const int c0 = (int)((8 * i) % C_out);
+        uint4 o;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float2 t = make_float2(v[2 * j], v[2 * j + 1]);
+            if (epilogue)
+                t = silu_f32x2(ffma2(t, make_float2(__ldg(scale + c0 + 2 * j), __ldg(scale + c0 + 2 * j + 1)),
+                                     make_float2(__ldg(bias + c0 + 2 * j), __ldg(bias + c0 + 2 * j + 1))));
+            h[j] = __floats2bfloat162_rn(t.x, t.y);
+        }
+        reinterpret_cast<uint4 *>(y)[i] = o;
+    }
+}
+}  // namespace
+
+cudaError_t launch_splitk_reduce(const float *ws, int splits, int64_t M, int C_out, const float *scale,
+                                 const float *bias, void *y, int epilogue, cudaStream_t st)
+{
+    const int64_t MC = M * C_out;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, splitk_reduce_kernel, 256, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    int64_t grid = (MC / 8 + 255) / 256;
+    if (grid > (int64_t)sm_count() * per_sm) grid = (int64_t)sm_count() * per_sm;
+    splitk_reduce_kernel<<<(unsigned)grid, 256, 0, st>>>(ws, splits, MC, C_out, scale, bias,
+                                                         reinterpret_cast<__nv_bfloat16 *>(y), epilogue);
+    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- wait probe

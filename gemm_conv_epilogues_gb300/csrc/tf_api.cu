@@ -138,6 +138,40 @@ int run_conv(const void *x, const void *w, const float *scale, const float *bias
 
 bool bad_rows_cols(int64_t rows, int64_t cols) { return rows <= 0 || cols <= 0; }
 
+// Split-K bytes for a shape the dispatch sends to the tensor-core kernel
+// (0 when it would not split).
+int64_t splitk_bytes(const tf_conv_shape &s, int Ho, int Wo, int *splits)
+{
+    *splits = 1;
+    if (select_variant(s, Ho, Wo) != TF_CONV_UMMA) return 0;
+    const int S = conv_umma_splits(s, Ho, Wo);
+    if (S <= 1) return 0;
+    *splits = S;
+    return (int64_t)S * s.N * Ho * Wo * s.C_out * 4;
+}
+
+int run_conv_ws(const void *x, const void *w, const float *scale, const float *bias, void *y,
+                const tf_conv_shape *shape, void *ws, int64_t ws_bytes, cudaStream_t st)
+{
+    int Ho = 0, Wo = 0;
+    if (!x || !w || !y || !shape || !scale || !bias || ws_bytes < 0 || (ws_bytes > 0 && !ws))
+        return TF_ERR_INVALID_ARG;
+    int rc = check_conv_shape(shape, &Ho, &Wo);
+    if (rc != TF_OK) return rc;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (ws && !aligned16(ws))) return TF_ERR_UNSUPPORTED;
+    int splits = 1;
+    const int64_t need = splitk_bytes(*shape, Ho, Wo, &splits);
+    if (need == 0 || need > ws_bytes) return run_conv(x, w, scale, bias, y, shape, TF_CONV_AUTO, 1, st);
+    if (!aligned16(scale) || !aligned16(bias)) return TF_ERR_UNSUPPORTED;
+    ConvArgs a{x, w, scale, bias, y, *shape, Ho, Wo, 1};
+    a.splits = splits;
+    a.ws = static_cast<float *>(ws);
+    rc = from_cuda(launch_conv_umma(a, st));
+    if (rc != TF_OK) return rc;
+    const int64_t M = (int64_t)shape->N * Ho * Wo;
+    return from_cuda(launch_splitk_reduce(a.ws, splits, M, shape->C_out, scale, bias, y, 1, st));
+}
+
 }  // namespace
 
 extern "C" {
@@ -171,6 +205,20 @@ int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *sc
 {
     if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA) return TF_ERR_INVALID_ARG;
     return run_conv(x, w_ohwi, scale, bias, y, shape, variant, 1, (cudaStream_t)stream);
+}
+
+int64_t tf_conv2d_bn_silu_workspace_size(const tf_conv_shape *shape)
+{
+    int Ho = 0, Wo = 0;
+    if (check_conv_shape(shape, &Ho, &Wo) != TF_OK) return 0;
+    int splits = 1;
+    return splitk_bytes(*shape, Ho, Wo, &splits);
+}
+
+int tf_conv2d_bn_silu_ws(const void *x, const void *w_ohwi, const float *scale, const float *bias, void *y,
+                         const tf_conv_shape *shape, void *workspace, int64_t workspace_bytes, tf_stream_t stream)
+{
+    return run_conv_ws(x, w_ohwi, scale, bias, y, shape, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 int tf_conv2d_bn_silu_select(const tf_conv_shape *shape)

@@ -27,12 +27,19 @@ struct ConvArgs {
     tf_conv_shape s;
     int Ho, Wo;
     int epilogue;
+    int splits = 1;          // tensor-core kernel only: K splits, fp32 partials to ws
+    float *ws = nullptr;
 };
 cudaError_t launch_conv_direct(const ConvArgs &a, cudaStream_t st);
 cudaError_t launch_conv_tiled(const ConvArgs &a, cudaStream_t st);
 // Returns cudaErrorNotSupported when the shape does not fit the kernel.
 cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st);
 bool conv_umma_supports(const tf_conv_shape &s, int Ho, int Wo);
+// K splits worth using for this shape (1: none), and the reduction that sums
+// the splits' fp32 partials and applies the epilogue.
+int conv_umma_splits(const tf_conv_shape &s, int Ho, int Wo);
+cudaError_t launch_splitk_reduce(const float *ws, int splits, int64_t M, int C_out, const float *scale,
+                                 const float *bias, void *y, int epilogue, cudaStream_t st);
 
 cudaError_t launch_pack_filter(const void *w_oihw, void *w_ohwi, int C_out, int C_in, int KH, int KW,
                                cudaStream_t st);

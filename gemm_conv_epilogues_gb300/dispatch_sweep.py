@@ -8,7 +8,8 @@ check that they still hold).
 
 Every variant is timed with CUDA events around replays of a CUDA graph of
 back-to-back calls (median of 5 replays), so the numbers are GPU time, not
-host launch cost; shapes a variant cannot take are skipped.  The last
+host launch cost; shapes a variant cannot take are skipped.  "umma+splitk"
+is tf_conv2d_bn_silu_ws with a full workspace, for shapes it splits.  The last
 column is the kernel the library's dispatch picks today, so a row where it
 differs from the fastest one shows a threshold to revisit.
 """
@@ -80,6 +81,10 @@ def run(quick: bool = False):
             if b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v, check=False) != b.TF_OK:
                 continue
             t[NAMES[v]] = _time_us(lambda v=v: b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v), reps)
+        need = b.tf_conv2d_bn_silu_workspace_size(shape)
+        if need > 0:
+            ws = torch.empty((need // 4,), dtype=torch.float32, device=dev)
+            t["umma+splitk"] = _time_us(lambda: b.tf_conv2d_bn_silu_ws(x, w, sc, bi, y, shape, ws, need), reps)
         rows.append({"N": c.N, "H": c.H, "W": c.W, "C_in": c.C_in, "C_out": c.C_out, "K": c.KH,
                      "M": c.M, "mflop": c.flops / 1e6, "us": t, "best": min(t, key=t.get),
                      "dispatch": NAMES[b.tf_conv2d_bn_silu_select(shape)]})
@@ -90,12 +95,12 @@ def run(quick: bool = False):
 
 
 def markdown(rows) -> str:
-    out = ["| N,H,W | C_in | C_out | k | MFLOP | direct us | tiled us | umma us | fastest | dispatch |",
-           "|---|---:|---:|---:|---:|---:|---:|---:|---|---|"]
+    out = ["| N,H,W | C_in | C_out | k | MFLOP | direct us | tiled us | umma us | umma+splitk us | fastest | dispatch |",
+           "|---|---:|---:|---:|---:|---:|---:|---:|---:|---|---|"]
     for r in rows:
         f = lambda k: f"{r['us'][k]:.1f}" if k in r["us"] else "-"
         out.append(f"| {r['N']},{r['H']},{r['W']} | {r['C_in']} | {r['C_out']} | {r['K']} | {r['mflop']:.1f} | "
-                   f"{f('direct')} | {f('tiled')} | {f('umma')} | {r['best']} | {r['dispatch']} |")
+                   f"{f('direct')} | {f('tiled')} | {f('umma')} | {f('umma+splitk')} | {r['best']} | {r['dispatch']} |")
     agree = sum(r["best"] == r["dispatch"] for r in rows)
     out.append(f"\ndispatch picks the fastest kernel in {agree} of {len(rows)} shapes")
     return "\n".join(out)

@@ -138,6 +138,25 @@ WORKLOADS = {
 }
 
 
+# Producer -> consumer pair ("When the fusion you want is impossible, fuse into
+# the producer"): a pointwise activation between two convolutions, the
+# consumer a 7x7 conv.  Producer: 1x1, 256 -> 128 channels; consumer: 7x7,
+# 128 -> 128, pad 3, both on 16 x 64 x 64 NHWC bf16.
+PAIR_PRODUCER = ConvShape(16, 64, 64, 256, 128, 1, 1, (1, 1), (0, 0))
+PAIR_CONSUMER = ConvShape(16, 64, 64, 128, 128, 7, 7, (1, 1), (3, 3))
+
+
+def producer_consumer_inputs(producer: ConvShape, consumer: ConvShape, seed: int = 0) -> dict:
+    """Inputs of both convs: the producer's x, w, scale, bias (streams 0..3)
+    and the consumer's w, scale, bias (streams 11..13), weights N(0, var 1/fan_in)."""
+    a = conv_inputs(producer, seed, "normal_fanin")
+    c = consumer
+    w2 = _normal(_rng(seed, 11), (c.C_out, c.C_in, c.KH, c.KW), 1.0 / np.sqrt(c.KH * c.KW * c.C_in))
+    return {"x": a["x"], "w1_oihw": a["w_oihw"], "scale1": a["scale"], "bias1": a["bias"],
+            "w2_oihw": f32_to_bf16_bits(w2), "scale2": _uniform(_rng(seed, 12), (c.C_out,), 0.5, 1.5),
+            "bias2": _normal(_rng(seed, 13), (c.C_out,), 0.1)}
+
+
 def workload_inputs(w: Workload, seed: int = 0) -> dict:
     if w.kind == "conv":
         return conv_inputs(w.conv, seed, w.w_dist)

@@ -120,6 +120,26 @@ int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *sc
                               const float *bias, void *y, const tf_conv_shape *shape,
                               int variant, tf_stream_t stream);
 
+/* Bytes of device workspace tf_conv2d_bn_silu_ws can use for this shape: the
+ * fp32 partial sums of a K split, splits * N*Ho*Wo * C_out * 4 bytes, or 0
+ * when the shape fills the GPU without splitting (or is invalid).  Host only. */
+int64_t tf_conv2d_bn_silu_workspace_size(const tf_conv_shape *shape);
+
+/* Same result as tf_conv2d_bn_silu, with a caller-owned device workspace.
+ * When the tensor-core kernel would leave SMs idle (fewer 128 x BN output
+ * tiles than half the SMs) it splits the K loop (filter taps x input
+ * channels) across CTAs -- the tile size and split chosen from the layer
+ * shape and the SM count ("Fusing an Epilogue", "Three kernels for one
+ * operation") -- writes fp32 partial sums to `workspace`, and a second kernel
+ * adds them and applies the BatchNorm + SiLU epilogue.  With a workspace
+ * smaller than tf_conv2d_bn_silu_workspace_size (including 0) it runs
+ * tf_conv2d_bn_silu unchanged.  The workspace must be 16-byte aligned, must
+ * not alias x, w, y, and is in use until the stream reaches the end of the
+ * call; concurrent calls need separate workspaces. */
+int tf_conv2d_bn_silu_ws(const void *x, const void *w_ohwi, const float *scale, const float *bias,
+                         void *y, const tf_conv_shape *shape, void *workspace,
+                         int64_t workspace_bytes, tf_stream_t stream);
+
 /* The kernel tf_conv2d_bn_silu would run for this shape (host only, launches
  * nothing), or a negative tf_status value when the shape is rejected.
  * "Fusing an Epilogue", "Three kernels for one operation": the lowering picks

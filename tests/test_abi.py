@@ -96,6 +96,21 @@ def test_host_validation_rejects_before_launch(native_lib):
     assert b.tf_unfused_affine(p16, p16, p16, None, 2, 8, 0, check=False) == S
 
 
+def test_split_k_workspace_size(native_lib):
+    from gemm_conv_epilogues_gb300 import binding as b, synth
+    big = synth.WORKLOADS["conv7x7_16x64x64x512_to512"].conv
+    assert b.tf_conv2d_bn_silu_workspace_size(b.conv_shape(big.N, big.H, big.W, big.C_in, big.C_out, 7, 7,
+                                                           (1, 1), (3, 3))) == 0
+    small = b.conv_shape(1, 16, 16, 256, 256, 3, 3, (1, 1), (1, 1))      # 2 output tiles, 36 K blocks
+    need = b.tf_conv2d_bn_silu_workspace_size(small)
+    assert need > 0 and need % (256 * 256 * 4) == 0
+    assert b.tf_conv2d_bn_silu_workspace_size(b.conv_shape(1, 16, 16, 8, 16, 3, 3, (1, 1), (1, 1))) == 0
+    p16 = 1 << 20
+    assert b.tf_conv2d_bn_silu_ws(p16, p16, p16, p16, p16, small, None, 64, 0, check=False) == b.TF_ERR_INVALID_ARG
+    assert b.tf_conv2d_bn_silu_ws(p16, p16, p16, p16, p16, small, p16 + 8, need, 0, check=False) == \
+        b.TF_ERR_UNSUPPORTED
+
+
 def test_dispatch_selects_by_shape(native_lib):
     from gemm_conv_epilogues_gb300 import binding as b, synth
     w = synth.WORKLOADS

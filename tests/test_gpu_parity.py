@@ -117,6 +117,33 @@ def test_conv_umma_small(b, c):
     _assert_no_device_error(b)
 
 
+SPLITK_SHAPES = [
+    synth.ConvShape(1, 16, 16, 256, 256, 3, 3, (1, 1), (1, 1)),     # 2 tiles, 36 K blocks
+    synth.ConvShape(1, 8, 8, 512, 128, 3, 3, (1, 1), (1, 1)),       # one ragged tile
+    synth.ConvShape(2, 14, 14, 128, 64, 7, 7, (1, 1), (3, 3)),      # 7x7, ragged M tail
+    synth.ConvShape(1, 12, 12, 1024, 512, 1, 1, (1, 1), (0, 0)),    # 1x1, 2 N tiles, 16 K blocks
+]
+
+
+@pytest.mark.parametrize("c", SPLITK_SHAPES, ids=lambda c: f"{c.N}x{c.H}x{c.W}x{c.C_in}-{c.C_out}k{c.KH}")
+def test_conv_split_k_workspace(b, c):
+    d = synth.conv_inputs(c, seed=15, w_dist="normal_fanin")
+    shape = _shape(b, c)
+    need = b.tf_conv2d_bn_silu_workspace_size(shape)
+    assert need > 0, "shape expected to split"
+    ws = torch.full((need // 4,), float("nan"), dtype=torch.float32, device="cuda")   # every partial must be written
+    x = dev_u16(d["x"])
+    w = torch.empty((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device="cuda")
+    b.tf_pack_filter_nhwc(dev_u16(d["w_oihw"]), w, c.C_out, c.C_in, c.KH, c.KW)
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    for nbytes in (need, need - 16, 0):   # split, then too small a workspace: the unsplit path
+        y = torch.full((c.M, c.C_out), 0x7FC0, dtype=torch.int16, device="cuda")
+        b.tf_conv2d_bn_silu_ws(x, w, dev_f32(d["scale"]), dev_f32(d["bias"]), y, shape, ws if nbytes else None, nbytes)
+        torch.cuda.synchronize()
+        _conv_check(bf16_to_f64(host_u16(y)).reshape(ref.shape), ref)
+    _assert_no_device_error(b)
+
+
 def test_conv_umma_plain_epilogue_is_the_bare_conv(b):
     c = synth.ConvShape(2, 12, 12, 64, 64, 3, 3, (1, 1), (1, 1))
     d = synth.conv_inputs(c, seed=3, w_dist="normal_fanin")
@@ -147,6 +174,40 @@ def test_conv_full_workload_sampled(b, name, nrand):
     _conv_check(got[pts], ref)
     assert np.isfinite(got).all()
     _assert_no_device_error(b)
+
+
+# ---------------------------------------------------------------- producer -> consumer convs
+
+@pytest.mark.parametrize("standalone", [False, True])
+def test_producer_consumer_pair(b, standalone):
+    # a 1x1 producer, BN+SiLU, then a 7x7 consumer: the activation either in
+    # the producer's epilogue or as separate BN and SiLU kernels
+    p = synth.ConvShape(2, 12, 12, 128, 64, 1, 1, (1, 1), (0, 0))
+    c = synth.ConvShape(2, 12, 12, 64, 64, 7, 7, (1, 1), (3, 3))
+    d = synth.producer_consumer_inputs(p, c, seed=14)
+    w1 = torch.empty((p.C_out, 1, 1, p.C_in), dtype=torch.int16, device="cuda")
+    w2 = torch.empty((c.C_out, 7, 7, c.C_in), dtype=torch.int16, device="cuda")
+    b.tf_pack_filter_nhwc(dev_u16(d["w1_oihw"]), w1, p.C_out, p.C_in, 1, 1)
+    b.tf_pack_filter_nhwc(dev_u16(d["w2_oihw"]), w2, c.C_out, c.C_in, 7, 7)
+    s1, b1, s2, b2 = (dev_f32(d[k]) for k in ("scale1", "bias1", "scale2", "bias2"))
+    x = dev_u16(d["x"])
+    u = torch.empty((p.M, p.C_out), dtype=torch.int16, device="cuda")
+    y = torch.empty((c.M, c.C_out), dtype=torch.int16, device="cuda")
+    if standalone:
+        t1, t2 = torch.empty_like(u), torch.empty_like(u)
+        b.tf_unfused_conv2d(x, w1, t1, _shape(b, p), b.TF_CONV_UMMA)
+        b.tf_unfused_bn(t1, s1, b1, t2, p.M, p.C_out)
+        b.tf_unfused_silu(t2, u, p.M * p.C_out)
+    else:
+        b.tf_conv2d_bn_silu_variant(x, w1, s1, b1, u, _shape(b, p), b.TF_CONV_UMMA)
+    b.tf_conv2d_bn_silu_variant(u, w2, s2, b2, y, _shape(b, c), b.TF_CONV_UMMA)
+    torch.cuda.synchronize()
+    epi = oracle.EPI_CHAIN if standalone else oracle.EPI_FUSED
+    u_ref = oracle.conv2d_bn_silu(d["x"], d["w1_oihw"], d["scale1"], d["bias1"], p.stride, p.pad, epi)
+    u_bits = synth.f32_to_bf16_bits(u_ref.astype(np.float32))       # the stored intermediate
+    y_ref = oracle.conv2d_bn_silu(u_bits, d["w2_oihw"], d["scale2"], d["bias2"], c.stride, c.pad)
+    _conv_check(bf16_to_f64(host_u16(u)).reshape(u_ref.shape), u_ref)
+    _conv_check(bf16_to_f64(host_u16(y)).reshape(y_ref.shape), y_ref)
 
 
 # ---------------------------------------------------------------- bias + GELU
