@@ -46,6 +46,7 @@ _SIGS = {
     "tf_conv2d_bn_silu_select": ([ctypes.POINTER(tf_conv_shape)], _i),
     "tf_conv2d_bn_silu_workspace_size": ([ctypes.POINTER(tf_conv_shape)], _i64),
     "tf_conv2d_bn_silu_ws": ([_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(tf_conv_shape), _vp, _i64, _vp], _i),
+    "tf_conv2d_bn_silu_static_ws": ([_vp, _vp, _vp, _vp, _vp, ctypes.POINTER(tf_conv_shape), _vp], _i),
     "tf_bias_gelu": ([_vp, _vp, _vp, _i64, _i64, _vp], _i),
     "tf_bias_gelu_rowsum": ([_vp, _vp, _vp, _vp, _i64, _i64, _vp], _i),
     "tf_unfused_rowsum": ([_vp, _vp, _i64, _i64, _vp], _i),
@@ -137,6 +138,15 @@ def tf_conv2d_bn_silu_ws(x, w_ohwi, scale, bias, y, shape, workspace, workspace_
     return _check(_lib.tf_conv2d_bn_silu_ws(_ptr(x), _ptr(w_ohwi), _ptr(scale), _ptr(bias), _ptr(y),
                                             ctypes.byref(shape), _ptr(workspace), int(workspace_bytes),
                                             _stream(stream)), "tf_conv2d_bn_silu_ws", check)
+
+
+def tf_conv2d_bn_silu_static_ws(x, w_ohwi, scale, bias, y, shape, stream=None, check=True):
+    """tf_conv2d_bn_silu_ws without a workspace argument, for callers that cannot
+    allocate device memory: the split-K partials use the library's one 8 MiB
+    static device array (calls that overlap on the GPU race on it)."""
+    return _check(_lib.tf_conv2d_bn_silu_static_ws(_ptr(x), _ptr(w_ohwi), _ptr(scale), _ptr(bias), _ptr(y),
+                                                   ctypes.byref(shape), _stream(stream)),
+                  "tf_conv2d_bn_silu_static_ws", check)
 
 
 def tf_bias_gelu(x, bias, y, rows, cols, stream=None, check=True):

@@ -140,6 +140,30 @@ int tf_conv2d_bn_silu_ws(const void *x, const void *w_ohwi, const float *scale, 
                          void *y, const tf_conv_shape *shape, void *workspace,
                          int64_t workspace_bytes, tf_stream_t stream);
 
+/* tf_conv2d_bn_silu_ws for callers that cannot allocate device memory (no
+ * counterpart in the pages: it exists for callers such as a serving runtime
+ * or plugin host that plans and owns every device buffer, or code that must
+ * not call cudaMalloc on the request path because it can synchronise the
+ * device or fail when memory is fragmented).  Same arguments and result as
+ * tf_conv2d_bn_silu, no workspace argument: the split-K partial sums go to
+ * one library-owned device array of 8 MiB (8388608 bytes), a static
+ * __device__ allocation that every GPU loading the library keeps until the
+ * process exits.  The call allocates nothing.
+ *   - Returns TF_ERR_UNSUPPORTED, launching nothing, when the shape's
+ *     partial sums (tf_conv2d_bn_silu_workspace_size) exceed 8 MiB; shapes
+ *     that do not split run unsplit, as tf_conv2d_bn_silu.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (every split rewrites all its partials before they are read, so
+ *     nothing needs clearing).  Calls whose GPU work overlaps -- on
+ *     different streams or from different host threads without ordering --
+ *     race on it; issue them on one stream. */
+int tf_conv2d_bn_silu_static_ws(const void *x, const void *w_ohwi, const float *scale,
+                                const float *bias, void *y, const tf_conv_shape *shape,
+                                tf_stream_t stream);
+
 /* The kernel tf_conv2d_bn_silu would run for this shape (host only, launches
  * nothing), or a negative tf_status value when the shape is rejected.
  * "Fusing an Epilogue", "Three kernels for one operation": the lowering picks
