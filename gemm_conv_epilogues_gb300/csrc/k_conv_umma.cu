@@ -68,7 +68,13 @@ struct UmmaParams {
     float *ws;               // split-K partials [splits][M][C_out] (epilogue 2 only)
 };
 
-template <int BN, bool IM2COL>
+// CL: CTAs per cluster along M (1 or 2).  With CL = 2 the two CTAs of a
+// cluster take vertically adjacent output tiles that share the same filter
+// (B) tile; each loads half of B and multicasts it to both, and each MMA
+// thread's stage release is multicast to both producers, so a stage is
+// refilled only after both CTAs have consumed it.  Every SM then fetches
+// 16 KB of A + BN*64 B of B per 64-deep K step instead of 16 KB + BN*128 B.
+template <int BN, bool IM2COL, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_umma_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_y, const UmmaParams p)
@@ -84,11 +90,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int crank = CL > 1 ? (int)ptx::cluster_ctarank() : 0;
+    const int cid = (int)blockIdx.x / CL, ncl = (int)gridDim.x / CL;   // cluster index and count
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&empty[s], CL);   // released by the MMA thread of every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&tfull[b], 1);
@@ -107,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    if constexpr (CL > 1) ptx::cluster_sync();   // peers' barriers exist before any multicast
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
@@ -116,11 +125,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued = 0, last_phase = 0;  // per-stage bit masks
             bool ok = true;
-            for (int work = blockIdx.x; ok && work < p.num_work; work += gridDim.x) {
+            for (int work = cid; ok && work < p.num_work; work += ncl) {
                 const int tile = work / p.splits;
                 const int kb_begin = (work - tile * p.splits) * p.kb_per_split;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
-                const int m0 = (tile / p.num_n_tiles) * BM;
+                const int m0 = ((tile / p.num_n_tiles) * CL + crank) * BM;
                 const int n0 = (tile % p.num_n_tiles) * BN;
                 const int img = m0 / p.HoWo;
                 const int rem = m0 - img * p.HoWo;
@@ -143,7 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         ptx::tma_load_2d(a_dst, &tmap_a, &full[stage], c0, m0);
                     }
-                    ptx::tma_load_2d(b_dst, &tmap_b, &full[stage], kb * BK, n0);
+                    if constexpr (CL > 1)
+                        ptx::tma_load_2d_multicast(b_dst + crank * (BN / CL) * (BK * 2), &tmap_b, &full[stage],
+                                                   kb * BK, n0 + crank * (BN / CL), (uint16_t)((1u << CL) - 1));
+                    else
+                        ptx::tma_load_2d(b_dst, &tmap_b, &full[stage], kb * BK, n0);
                     issued |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
@@ -167,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int work = blockIdx.x; ok && work < p.num_work; work += gridDim.x, ++local) {
+            for (int work = cid; ok && work < p.num_work; work += ncl, ++local) {
                 const int kb_begin = (work % p.splits) * p.kb_per_split;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
                 const int b = local & 1;
@@ -192,7 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2), idesc,
                                        (kb > kb_begin || k > 0) ? 1u : 0u);
                     }
-                    ptx::umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+                    // frees the stage (in every CTA of the cluster) once these MMAs have read it
+                    if constexpr (CL > 1)
+                        ptx::umma_commit_multicast(&empty[stage], (uint16_t)((1u << CL) - 1));
+                    else
+                        ptx::umma_commit(&empty[stage]);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -217,10 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *stage_out = smem + L::OUT_OFFSET + (warp - 2) * 2 * kOutBoxBytes;
         int local = 0, nstore = 0;
         bool ok = true;
-        for (int work = blockIdx.x; work < p.num_work; work += gridDim.x, ++local) {
+        for (int work = cid; work < p.num_work; work += ncl, ++local) {
             const int tile = work / p.splits;
             const int split = work - tile * p.splits;
-            const int m0 = (tile / p.num_n_tiles) * BM;
+            const int m0 = ((tile / p.num_n_tiles) * CL + crank) * BM;
             const int n0 = (tile % p.num_n_tiles) * BN;
             const int b = local & 1;
             const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
@@ -300,6 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    // no CTA exits while its peer may still multicast into it or release its stages
+    if constexpr (CL > 1) ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
@@ -358,29 +377,54 @@ bool is_plain_gemm(const tf_conv_shape &s)
 // positions ow*stride - pad.
 int upper_corner(int in, int out, int stride, int pad) { return (out - 1) * stride - pad - (in - 1); }
 
-template <int BN, bool IM2COL>
-cudaError_t launch_bn(const ConvArgs &a, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
-                      const UmmaParams &p, cudaStream_t st)
+template <int BN, bool IM2COL, int CL>
+cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty, const UmmaParams &p,
+                      cudaStream_t st)
 {
     using L = Layout<BN>;
+    auto kern = conv_umma_kernel<BN, IM2COL, CL>;
     // Per-function, per-device attribute; cheap enough to set on every launch.
-    cudaError_t e = cudaFuncSetAttribute(conv_umma_kernel<BN, IM2COL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    const int grid = p.num_work < sm_count() ? p.num_work : sm_count();
-    conv_umma_kernel<BN, IM2COL><<<grid, kThreads, L::ALLOC, st>>>(ta, tb, ty, p);
-    return cudaGetLastError();
+    if constexpr (CL == 1) {
+        const int grid = p.num_work < sm_count() ? p.num_work : sm_count();
+        kern<<<grid, kThreads, L::ALLOC, st>>>(ta, tb, ty, p);
+        return cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CL;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = L::ALLOC;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // persistent: as many clusters as can be resident at once (an SM left
+        // without a partner in its GPC stays idle rather than starting a
+        // second wave)
+        cfg.gridDim = dim3(sm_count() / CL * CL);
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (clusters < 1) return cudaErrorNotSupported;
+        if (clusters > p.num_work) clusters = p.num_work;
+        cfg.gridDim = dim3(CL * clusters);
+        return cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
+    }
 }
 
-template <bool IM2COL>
-cudaError_t launch_im(int bn, const ConvArgs &a, const CUtensorMap &ta, const CUtensorMap &tb,
-                      const CUtensorMap &ty, const UmmaParams &p, cudaStream_t st)
+template <bool IM2COL, int CL>
+cudaError_t launch_im(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
+                      const UmmaParams &p, cudaStream_t st)
 {
     switch (bn) {
-    case 256: return launch_bn<256, IM2COL>(a, ta, tb, ty, p, st);
-    case 128: return launch_bn<128, IM2COL>(a, ta, tb, ty, p, st);
-    case 64: return launch_bn<64, IM2COL>(a, ta, tb, ty, p, st);
-    case 32: return launch_bn<32, IM2COL>(a, ta, tb, ty, p, st);
+    case 256: return launch_bn<256, IM2COL, CL>(ta, tb, ty, p, st);
+    case 128: return launch_bn<128, IM2COL, CL>(ta, tb, ty, p, st);
+    case 64: return launch_bn<64, IM2COL, CL>(ta, tb, ty, p, st);
+    case 32: return launch_bn<32, IM2COL, CL>(ta, tb, ty, p, st);
     default: return cudaErrorNotSupported;
     }
 }
@@ -411,6 +455,7 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     EncodeTiledFn tiled = encode_tiled();
     if (!tiled) return cudaErrorNotSupported;
     const int bn = pick_bn(s.C_out);
+    const int cl = a.cluster == 2 ? 2 : 1;
     const int64_t M = (int64_t)s.N * a.Ho * a.Wo;
     const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
 
@@ -425,10 +470,10 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    {   // B: packed filters as a [C_out][K] K-major matrix
+    {   // B: packed filters as a [C_out][K] K-major matrix (each CTA of a cluster loads BN/cl rows)
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)s.C_out};
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {BK, (cuuint32_t)bn};
+        const cuuint32_t box[2] = {BK, (cuuint32_t)(bn / cl)};
         const cuuint32_t estr[2] = {1, 1};
         if (tiled(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.w), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -478,7 +523,7 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     p.cblocks = s.C_in / BK;
     p.num_kb = (int)(K / BK);
     p.num_n_tiles = s.C_out / bn;
-    p.num_tiles = (int)((M + BM - 1) / BM) * p.num_n_tiles;
+    p.num_tiles = (int)(((M + BM - 1) / BM + cl - 1) / cl) * p.num_n_tiles;   // cl vertically adjacent tiles each
     p.epilogue = a.epilogue;
     p.splits = 1;
     p.kb_per_split = p.num_kb;
@@ -492,7 +537,8 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     }
     p.num_work = p.num_tiles * p.splits;
     if (p.err == nullptr) return cudaErrorInitializationError;
-    return im2col ? launch_im<true>(bn, a, ta, tb, ty, p, st) : launch_im<false>(bn, a, ta, tb, ty, p, st);
+    if (cl == 2) return im2col ? launch_im<true, 2>(bn, ta, tb, ty, p, st) : launch_im<false, 2>(bn, ta, tb, ty, p, st);
+    return im2col ? launch_im<true, 1>(bn, ta, tb, ty, p, st) : launch_im<false, 1>(bn, ta, tb, ty, p, st);
 }
 
 // ---------------------------------------------------------------- split K

@@ -294,25 +294,11 @@ __global__ void __launch_bounds__(256) layernorm_warp_kernel(const __half *__res
 
 // ---------------------------------------------------------------- a cluster per row
 
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t cluster_nctarank()
 {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
     return r;
-}
-
-// All threads of all CTAs of the cluster; orders shared-memory writes before
-// the barrier with reads of them (local or remote) after it.
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Reads a float from the same shared-memory variable in CTA `rank` of the cluster.
@@ -357,7 +343,7 @@ __global__ void __launch_bounds__(1024) layernorm_cluster_kernel(const __half *_
     constexpr int NV = 2;
     __shared__ float red[32];
     __shared__ float part[2];
-    const uint32_t rank = cluster_ctarank(), nranks = cluster_nctarank();
+    const uint32_t rank = ptx::cluster_ctarank(), nranks = cluster_nctarank();
     const int64_t row = blockIdx.x / nranks;
     const int c0 = (int)rank * slice;                    // first column of this CTA's slice
     const int nvec = (min(hidden - c0, slice)) >> 3;     // vectors in the slice
@@ -392,7 +378,7 @@ __global__ void __launch_bounds__(1024) layernorm_cluster_kernel(const __half *_
     const float inv_h = 1.0f / (float)hidden;
     float total = cta_sum(sum, red);
     if (threadIdx.x == 0) part[0] = total;
-    cluster_sync();
+    ptx::cluster_sync();
     total = 0.0f;
     for (uint32_t r = 0; r < nranks; ++r) total += ld_dsmem(&part[0], r);
     const float mean = total * inv_h;
@@ -409,10 +395,10 @@ __global__ void __launch_bounds__(1024) layernorm_cluster_kernel(const __half *_
     }
     float sqt = cta_sum(sq, red);
     if (threadIdx.x == 0) part[1] = sqt;
-    cluster_sync();
+    ptx::cluster_sync();
     sqt = 0.0f;
     for (uint32_t r = 0; r < nranks; ++r) sqt += ld_dsmem(&part[1], r);
-    cluster_sync();   // no CTA leaves while another may still read its `part`
+    ptx::cluster_sync();   // no CTA leaves while another may still read its `part`
     const float rstd = rsqrtf(sqt * inv_h + eps);
     __half *yr = y + row * hidden + c0;
 #pragma unroll

@@ -93,6 +93,32 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *map, uint64_t
         : "memory");
 }
 
+// 2-D tiled load multicast to the CTAs of the cluster in `mask`: the box lands
+// at the same shared-memory offset in each of them and completes `bytes` on
+// the mbarrier at the same offset in each.
+__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const void *map, uint64_t *bar, int c0, int c1,
+                                                      uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Barrier over all threads of all CTAs of the cluster (release/acquire).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // 4-D im2col load (NHWC tensor): starting pixel (w, h, n), channels from c,
 // filter-tap offsets (off_w, off_h) added to every pixel of the column.
 __device__ __forceinline__ void tma_load_im2col_4d(void *dst, const void *map, uint64_t *bar, int c, int w,
@@ -188,6 +214,17 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// Same, arriving on the mbarrier at this offset in every CTA of the cluster
+// in `mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
 }
 
 // 32 TMEM lanes x 32 consecutive 32-bit columns: lane i of the warp receives

@@ -129,8 +129,10 @@ int run_conv(const void *x, const void *w, const float *scale, const float *bias
     case TF_CONV_DIRECT: return from_cuda(launch_conv_direct(a, st));
     case TF_CONV_TILED: return from_cuda(launch_conv_tiled(a, st));
     case TF_CONV_UMMA:
+    case TF_CONV_UMMA_PAIR:
         if (!conv_umma_supports(*shape, Ho, Wo)) return TF_ERR_UNSUPPORTED;
         if (epilogue && (!aligned16(scale) || !aligned16(bias))) return TF_ERR_UNSUPPORTED;
+        a.cluster = variant == TF_CONV_UMMA_PAIR ? 2 : 1;
         return from_cuda(launch_conv_umma(a, st));
     default: return TF_ERR_INVALID_ARG;
     }
@@ -203,7 +205,7 @@ int tf_conv2d_bn_silu(const void *x, const void *w_ohwi, const float *scale, con
 int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *scale, const float *bias, void *y,
                               const tf_conv_shape *shape, int variant, tf_stream_t stream)
 {
-    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA) return TF_ERR_INVALID_ARG;
+    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA_PAIR) return TF_ERR_INVALID_ARG;
     return run_conv(x, w_ohwi, scale, bias, y, shape, variant, 1, (cudaStream_t)stream);
 }
 
@@ -281,7 +283,7 @@ int tf_residual_layernorm_select(int64_t hidden)
 int tf_unfused_conv2d(const void *x, const void *w_ohwi, void *t1, const tf_conv_shape *shape, int variant,
                       tf_stream_t stream)
 {
-    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA) return TF_ERR_INVALID_ARG;
+    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA_PAIR) return TF_ERR_INVALID_ARG;
     return run_conv(x, w_ohwi, nullptr, nullptr, t1, shape, variant, 0, (cudaStream_t)stream);
 }
 

@@ -29,6 +29,7 @@ struct ConvArgs {
     int epilogue;
     int splits = 1;          // tensor-core kernel only: K splits, fp32 partials to ws
     float *ws = nullptr;
+    int cluster = 1;         // tensor-core kernel only: 2 = CTA pairs sharing filter tiles by multicast
 };
 cudaError_t launch_conv_direct(const ConvArgs &a, cudaStream_t st);
 cudaError_t launch_conv_tiled(const ConvArgs &a, cudaStream_t st);

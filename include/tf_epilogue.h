@@ -62,7 +62,9 @@ typedef enum {
     TF_CONV_AUTO = -1,   /* dispatch by shape */
     TF_CONV_DIRECT = 0,  /* one output element per thread, CUDA-core fp32 */
     TF_CONV_TILED = 1,   /* output-space tiles with a shared-memory halo, CUDA cores */
-    TF_CONV_UMMA = 2     /* implicit GEMM: TMA im2col -> tcgen05.mma -> TMEM -> fused epilogue */
+    TF_CONV_UMMA = 2,    /* implicit GEMM: TMA im2col -> tcgen05.mma -> TMEM -> fused epilogue */
+    TF_CONV_UMMA_PAIR = 3 /* the same on 2-CTA clusters: vertically adjacent output tiles share
+                             each filter tile, loaded half by each CTA and multicast to both */
 } tf_conv_variant;
 
 /* Row-reduction strategies of the LayerNorm kernels (see
@@ -113,7 +115,7 @@ int tf_conv2d_bn_silu(const void *x, const void *w_ohwi, const float *scale, con
 
 /* Same as tf_conv2d_bn_silu with the kernel forced (TF_CONV_*).  Returns
  * TF_ERR_UNSUPPORTED when the forced kernel cannot take the shape
- * (TF_CONV_UMMA needs C_in % 64 == 0, C_out % 32 == 0, and either a 1x1
+ * (TF_CONV_UMMA and TF_CONV_UMMA_PAIR need C_in % 64 == 0, C_out % 32 == 0, and either a 1x1
  * stride-1 unpadded filter or equal kernel extent, stride and padding along
  * H and W with padding <= 128 and stride <= 8). */
 int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *scale,

@@ -108,10 +108,11 @@ UMMA_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("variant", [2, 3], ids=["cta", "pair"])
 @pytest.mark.parametrize("c", UMMA_SHAPES, ids=lambda c: f"{c.N}x{c.H}x{c.W}x{c.C_in}-{c.C_out}k{c.KH}s{c.stride[0]}p{c.pad[0]}")
-def test_conv_umma_small(b, c):
+def test_conv_umma_small(b, c, variant):
     d = synth.conv_inputs(c, seed=2, w_dist="normal_fanin")
-    got = _run_conv(b, c, d, b.TF_CONV_UMMA)
+    got = _run_conv(b, c, d, variant)
     ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
     _conv_check(got, ref)
     _assert_no_device_error(b)
@@ -163,12 +164,13 @@ def test_conv_dispatch_tiny_workload(b):
 
 # ---------------------------------------------------------------- conv, full workloads, sampled
 
+@pytest.mark.parametrize("variant", [-1, 2, 3], ids=["auto", "cta", "pair"])
 @pytest.mark.parametrize("name,nrand", [("conv1x1_32x56x56x256_to256", 6000), ("conv7x7_16x64x64x512_to512", 1500)])
-def test_conv_full_workload_sampled(b, name, nrand):
+def test_conv_full_workload_sampled(b, name, nrand, variant):
     w = synth.WORKLOADS[name]
     c = w.conv
     d = synth.workload_inputs(w)
-    got = _run_conv(b, c, d, b.TF_CONV_AUTO).reshape(-1)
+    got = _run_conv(b, c, d, variant).reshape(-1)
     pts = conv_sample_points(c.N, c.Ho, c.Wo, c.C_out, nrand, seed=4)
     ref = oracle.conv2d_bn_silu_points(d["x"], d["w_oihw"], d["scale"], d["bias"], pts, c.stride, c.pad)
     _conv_check(got[pts], ref)
