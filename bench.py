@@ -107,32 +107,29 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def csrc_fingerprint() -> str:
-    """Hash of every kernel source and header: any change invalidates the
-    DRAM-traffic figures captured before it."""
-    import glob
+def files_fingerprint(files) -> str:
+    """Hash of the named kernel sources: a change to any of them invalidates
+    the DRAM-traffic figure captured before it."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "gemm_conv_epilogues_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(d, "*.cu")) + glob.glob(os.path.join(d, "*.h")) +
-                    glob.glob(os.path.join(d, "*.cuh"))):
-        h.update(os.path.basename(f).encode())
-        h.update(open(f, "rb").read())
+    for f in sorted(files):
+        h.update(f.encode())
+        h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def kernel_traffic(workload: str):
     """DRAM bytes (read + write) per launch of the workload's fused kernel from
-    the committed ncu summary, if no kernel source has changed since the
-    capture (else None)."""
+    the committed ncu summary, if none of the kernel's source files has
+    changed since the capture (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
-        t = json.load(open(path))
-        if t.get("csrc_sha256_16") != csrc_fingerprint():
+        e = json.load(open(path)).get(workload)
+        if not e or files_fingerprint(e["files"]) != e["files_sha256_16"]:
             return None
-        e = t["workloads"].get(workload)
-        return float(e["dram_bytes_per_launch"]) if e else None
+        return float(e["dram_bytes_per_launch"])
     except Exception:
         return None
 

@@ -52,7 +52,16 @@ def _fingerprint() -> str:
 
 
 def build_library(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link if the sources changed since the last build; return the .so path."""
+    """Compile and link if the sources changed since the last build; return the .so path.
+    Concurrent callers (parallel test workers) serialise on a lock file."""
+    import fcntl
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    with open(os.path.join(BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        return _build_locked(force, verbose)
+
+
+def _build_locked(force: bool, verbose: bool) -> str:
     stamp = LIB + ".stamp"
     fp = _fingerprint()
     if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == fp:

@@ -9,12 +9,12 @@
 // the padding), which is the TMA_LOAD_IM2COL -> UMMA path that page describes;
 // a 1x1 stride-1 unpadded convolution is a plain matrix, loaded as a 2-D tile.
 //
-// Persistent kernel, one CTA per SM, ten warps:
+// Persistent kernel, one CTA per SM, eighteen warps:
 //   warp 0  TMA producer: a ring of 4 shared-memory stages (A 16 KB + B BN*128 B)
 //   warp 1  TMEM allocator and MMA issuer: tcgen05.mma M=128, N=BN, K=16, fp32
 //           accumulators in TMEM, double-buffered so the epilogue of one tile
 //           overlaps the main loop of the next
-//   warps 2-9 epilogue ("Fusing an Epilogue", "The shape of it"): TMEM ->
+//   warps 2-17 epilogue ("Fusing an Epilogue", "The shape of it"): TMEM ->
 //           registers, v = acc*scale[co] + bias[co], v*sigmoid(v), bf16, then
 //           a swizzled shared-memory box and a TMA store.
 //           The per-channel parameters are read inside the kernel, as in the
@@ -35,18 +35,20 @@ constexpr int BM = 128;            // output pixels per tile (UMMA M)
 constexpr int BK = 64;             // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
 constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, each taking every other 32-column chunk
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// Epilogue warps: 16 (four per TMEM lane quarter) for short K loops, where the
+// epilogue paces the kernel; 8 for long ones, where it hides behind the MMAs.
+constexpr int kEpiWarpsShortK = 16, kEpiWarpsLongK = 8;
+constexpr int threads_for(int epi_warps) { return 64 + 32 * epi_warps; }
 constexpr int kOutBox = 32;        // epilogue store box: 32 pixels x 32 channels (64 B rows)
 constexpr int kOutBoxBytes = kOutBox * kOutBox * 2;
 
-template <int BN>
+template <int BN, int kEpiWarps>
 struct Layout {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int OUT_OFFSET = kStages * STAGE_BYTES;                 // 1024-aligned
-    static constexpr int OUT_BYTES = kEpiWarps * 2 * kOutBoxBytes;           // double-buffered per warp
+    static constexpr int OUT_BYTES = kEpiWarps * kOutBoxBytes;               // one staging box per warp
     static constexpr int BAR_OFFSET = OUT_OFFSET + OUT_BYTES;
     static constexpr int NUM_BARS = 2 * kStages + 5;  // full, empty, tmem full x2, tmem empty x2, drain
     static constexpr int TOTAL = BAR_OFFSET + NUM_BARS * 8 + 16;
@@ -74,12 +76,12 @@ struct UmmaParams {
 // thread's stage release is multicast to both producers, so a stage is
 // refilled only after both CTAs have consumed it.  Every SM then fetches
 // 16 KB of A + BN*64 B of B per 64-deep K step instead of 16 KB + BN*128 B.
-template <int BN, bool IM2COL, int CL>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, bool IM2COL, int CL, int kEpiWarps>
+__global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     conv_umma_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_y, const UmmaParams p)
 {
-    using L = Layout<BN>;
+    using L = Layout<BN, kEpiWarps>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFFSET);
@@ -225,14 +227,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         // Warp w reads TMEM lanes 32*(w%4) .. +31 (one output pixel per lane)
-        // and the 32-column chunks c = h, h+2, ... of the accumulator.  Each
+        // and the 32-column chunks c = h, h+4, ... of the accumulator.  Each
         // chunk becomes 32 pixels x 32 channels of bf16 in a 64-byte-swizzled
-        // staging box, written to y by one TMA store; two boxes per warp
-        // alternate so conversion overlaps the previous store.
+        // staging box, written to y by one TMA store.  Sixteen warps (four per
+        // SM sub-partition) keep the special-function and FMA pipes busy
+        // while others wait on TMEM loads and stores.
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
-        uint8_t *stage_out = smem + L::OUT_OFFSET + (warp - 2) * 2 * kOutBoxBytes;
-        int local = 0, nstore = 0;
+        uint8_t *box = smem + L::OUT_OFFSET + (warp - 2) * kOutBoxBytes;
+        int local = 0;
         bool ok = true;
         for (int work = cid; work < p.num_work; work += ncl, ++local) {
             const int tile = work / p.splits;
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int prow = m0 + q * 32;   // first pixel of this warp's rows
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
 #pragma unroll 1
-            for (int c = h; c < BN / 32; c += 2) {
+            for (int c = h; c < BN / 32; c += kEpiWarps / 4) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
                 if (p.epilogue == 2) {
@@ -266,31 +269,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     continue;
                 }
-                float sc[32], bi[32];
-                if (p.epilogue) {
-                    const float4 *s4 = reinterpret_cast<const float4 *>(p.scale + n0 + c * 32);
-                    const float4 *b4 = reinterpret_cast<const float4 *>(p.bias + n0 + c * 32);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float4 a4 = __ldg(s4 + j), c4 = __ldg(b4 + j);
-                        sc[4 * j] = a4.x; sc[4 * j + 1] = a4.y; sc[4 * j + 2] = a4.z; sc[4 * j + 3] = a4.w;
-                        bi[4 * j] = c4.x; bi[4 * j + 1] = c4.y; bi[4 * j + 2] = c4.z; bi[4 * j + 3] = c4.w;
-                    }
-                }
                 ptx::tmem_ld_wait();
                 uint32_t packed[16];
+                const float4 *s4 = reinterpret_cast<const float4 *>(p.scale + n0 + c * 32);
+                const float4 *b4 = reinterpret_cast<const float4 *>(p.bias + n0 + c * 32);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    float2 v = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                    if (p.epilogue)
-                        v = silu_f32x2(ffma2(v, make_float2(sc[2 * j], sc[2 * j + 1]),
-                                             make_float2(bi[2 * j], bi[2 * j + 1])));
-                    __nv_bfloat162 t = __floats2bfloat162_rn(v.x, v.y);
-                    packed[j] = *reinterpret_cast<uint32_t *>(&t);
+                for (int j = 0; j < 8; ++j) {
+                    float2 v0 = make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]));
+                    float2 v1 = make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    if (p.epilogue) {
+                        const float4 a4 = __ldg(s4 + j), c4 = __ldg(b4 + j);
+                        v0 = silu_f32x2(ffma2(v0, make_float2(a4.x, a4.y), make_float2(c4.x, c4.y)));
+                        v1 = silu_f32x2(ffma2(v1, make_float2(a4.z, a4.w), make_float2(c4.z, c4.w)));
+                    }
+                    __nv_bfloat162 t0 = __floats2bfloat162_rn(v0.x, v0.y), t1 = __floats2bfloat162_rn(v1.x, v1.y);
+                    packed[2 * j] = *reinterpret_cast<uint32_t *>(&t0);
+                    packed[2 * j + 1] = *reinterpret_cast<uint32_t *>(&t1);
                 }
-                uint8_t *box = stage_out + (nstore & 1) * kOutBoxBytes;
-                // the store issued from this box two chunks ago must have read it
-                if (lane == 0) ptx::bulk_wait_group_read<1>();
+                // the store issued from this box for the previous chunk must have read it
+                if (lane == 0) ptx::bulk_wait_group_read<0>();
                 __syncwarp();
                 // row `lane`, 16-byte chunk j lands at chunk j ^ ((lane >> 1) & 3):
                 // the 64-byte swizzle the store's tensor map expects
@@ -306,7 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (prow < p.M) ptx::tma_store_2d(&tmap_y, box, n0 + c * 32, prow);
                     ptx::bulk_commit_group();
                 }
-                ++nstore;
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&tempty[b]);
@@ -377,12 +373,13 @@ bool is_plain_gemm(const tf_conv_shape &s)
 // positions ow*stride - pad.
 int upper_corner(int in, int out, int stride, int pad) { return (out - 1) * stride - pad - (in - 1); }
 
-template <int BN, bool IM2COL, int CL>
+template <int BN, bool IM2COL, int CL, int EPI>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty, const UmmaParams &p,
                       cudaStream_t st)
 {
-    using L = Layout<BN>;
-    auto kern = conv_umma_kernel<BN, IM2COL, CL>;
+    using L = Layout<BN, EPI>;
+    constexpr int kThreads = threads_for(EPI);
+    auto kern = conv_umma_kernel<BN, IM2COL, CL, EPI>;
     // Per-function, per-device attribute; cheap enough to set on every launch.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
@@ -416,17 +413,27 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
     }
 }
 
+template <bool IM2COL, int CL, int EPI>
+cudaError_t launch_epi(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
+                       const UmmaParams &p, cudaStream_t st)
+{
+    switch (bn) {
+    case 256: return launch_bn<256, IM2COL, CL, EPI>(ta, tb, ty, p, st);
+    case 128: return launch_bn<128, IM2COL, CL, EPI>(ta, tb, ty, p, st);
+    case 64: return launch_bn<64, IM2COL, CL, EPI>(ta, tb, ty, p, st);
+    case 32: return launch_bn<32, IM2COL, CL, EPI>(ta, tb, ty, p, st);
+    default: return cudaErrorNotSupported;
+    }
+}
+
 template <bool IM2COL, int CL>
 cudaError_t launch_im(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
                       const UmmaParams &p, cudaStream_t st)
 {
-    switch (bn) {
-    case 256: return launch_bn<256, IM2COL, CL>(ta, tb, ty, p, st);
-    case 128: return launch_bn<128, IM2COL, CL>(ta, tb, ty, p, st);
-    case 64: return launch_bn<64, IM2COL, CL>(ta, tb, ty, p, st);
-    case 32: return launch_bn<32, IM2COL, CL>(ta, tb, ty, p, st);
-    default: return cudaErrorNotSupported;
-    }
+    // a work item of at most 16 K blocks finishes its MMAs in about the time
+    // the epilogue needs for the previous tile: give the epilogue more warps
+    if (p.kb_per_split <= 16) return launch_epi<IM2COL, CL, kEpiWarpsShortK>(bn, ta, tb, ty, p, st);
+    return launch_epi<IM2COL, CL, kEpiWarpsLongK>(bn, ta, tb, ty, p, st);
 }
 
 }  // namespace

@@ -138,64 +138,112 @@ __global__ void __launch_bounds__(kThreads) bias_gelu_kernel(const uint4 *__rest
 
 // ---------------------------------------------------------------- unfused pieces
 
-enum class Op { BiasAddF16, GeluF16, ResidualAddF16, BnBf16, SiluBf16 };
+enum class Op { BiasAddF16, GeluF16, ResidualAddF16, BnBf16, SiluBf16, AffineF16 };
 
-// One elementwise step of an unfused chain: reads one (or two) tensors,
-// writes one, all in the storage type of the chain.
+constexpr bool has_column_params(Op op) { return op == Op::BiasAddF16 || op == Op::BnBf16 || op == Op::AffineF16; }
+
+// Per-column parameters of one 16-byte vector (columns c0 .. c0+7): the fp16
+// bias (BiasAddF16), or the fp32 scale/gamma and bias/beta pairs.
 template <Op OP>
-__global__ void __launch_bounds__(kThreads) chain_kernel(const uint4 *__restrict__ a,
-                                                         const void *__restrict__ b,
-                                                         const float *__restrict__ scale,
-                                                         uint4 *__restrict__ out, int64_t nvec,
-                                                         int64_t cvec)
+__device__ __forceinline__ void column_params(const void *b, const float *p0, const float *p1, int64_t cv,
+                                              float (&m)[8], float (&a)[8])
 {
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nvec; i += stride) {
-        float f[8];
-        if constexpr (OP == Op::BiasAddF16) {
-            float g[8];
-            h8_to_f(ld_stream(a + i), f);
-            h8_to_f(__ldg(reinterpret_cast<const uint4 *>(b) + i % cvec), g);
+    if constexpr (OP == Op::BiasAddF16) {
+        h8_to_f(__ldg(reinterpret_cast<const uint4 *>(b) + cv), a);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) f[k] += g[k];
-            st_stream(out + i, f_to_h8(f));
-        } else if constexpr (OP == Op::GeluF16) {
-            h8_to_f(ld_stream(a + i), f);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) f[k] = gelu_f32(f[k]);
-            st_stream(out + i, f_to_h8(f));
-        } else if constexpr (OP == Op::ResidualAddF16) {
-            float g[8];
-            h8_to_f(ld_stream(a + i), f);
-            h8_to_f(ld_stream(reinterpret_cast<const uint4 *>(b) + i), g);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) f[k] += g[k];
-            st_stream(out + i, f_to_h8(f));
-        } else if constexpr (OP == Op::BnBf16) {
-            // b = bias, scale = scale, per channel c = (8*i) % C
-            b8_to_f(ld_stream(a + i), f);
-            const int64_t c0 = (i % cvec) * 8;
-            const float *bias = reinterpret_cast<const float *>(b);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) f[k] = f[k] * __ldg(scale + c0 + k) + __ldg(bias + c0 + k);
-            st_stream(out + i, f_to_b8(f));
-        } else {
-            b8_to_f(ld_stream(a + i), f);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) f[k] = silu_f32(f[k]);
-            st_stream(out + i, f_to_b8(f));
-        }
+        for (int k = 0; k < 8; ++k) m[k] = 1.0f;
+    } else if constexpr (OP == Op::BnBf16 || OP == Op::AffineF16) {
+        const float4 *q0 = reinterpret_cast<const float4 *>(p0 + 8 * cv);
+        const float4 *q1 = reinterpret_cast<const float4 *>(p1 + 8 * cv);
+        const float4 x0 = __ldg(q0), x1 = __ldg(q0 + 1), y0 = __ldg(q1), y1 = __ldg(q1 + 1);
+        m[0] = x0.x; m[1] = x0.y; m[2] = x0.z; m[3] = x0.w; m[4] = x1.x; m[5] = x1.y; m[6] = x1.z; m[7] = x1.w;
+        a[0] = y0.x; a[1] = y0.y; a[2] = y0.z; a[3] = y0.w; a[4] = y1.x; a[5] = y1.y; a[6] = y1.z; a[7] = y1.w;
     }
 }
 
 template <Op OP>
-cudaError_t launch_chain(const void *a, const void *b, const float *scale, void *out, int64_t n,
+__device__ __forceinline__ uint4 chain_op(const uint4 &va, const uint4 *bsrc, int64_t i, const float (&m)[8],
+                                          const float (&a)[8])
+{
+    float f[8];
+    if constexpr (OP == Op::BnBf16 || OP == Op::SiluBf16) b8_to_f(va, f);
+    else h8_to_f(va, f);
+    if constexpr (OP == Op::ResidualAddF16) {
+        float g[8];
+        h8_to_f(ld_stream(bsrc + i), g);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] += g[k];
+    } else if constexpr (OP == Op::GeluF16) {
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            const float2 t = gelu_f32x2(make_float2(f[k], f[k + 1]));
+            f[k] = t.x;
+            f[k + 1] = t.y;
+        }
+    } else if constexpr (OP == Op::SiluBf16) {
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            const float2 t = silu_f32x2(make_float2(f[k], f[k + 1]));
+            f[k] = t.x;
+            f[k + 1] = t.y;
+        }
+    } else if constexpr (OP == Op::BiasAddF16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] += a[k];
+    } else {   // BnBf16, AffineF16: f * m + a
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = fmaf(f[k], m[k], a[k]);
+    }
+    if constexpr (OP == Op::BnBf16 || OP == Op::SiluBf16) return f_to_b8(f);
+    else return f_to_h8(f);
+}
+
+// One elementwise step of an unfused chain: reads one (or two) tensors,
+// writes one, in the storage type of the chain (bf16 for the conv chain,
+// fp16 otherwise).  Built like bias_gelu_kernel -- grid-stride over 16-byte
+// vectors with a stride that is a multiple of the row length when it can be,
+// so per-column parameters stay in registers, and four loads in flight -- so
+// that the fused kernels are compared against equally careful kernels.
+template <Op OP>
+__global__ void __launch_bounds__(kThreads) chain_kernel(const uint4 *__restrict__ a, const void *__restrict__ b,
+                                                         const float *__restrict__ p0, const float *__restrict__ p1,
+                                                         uint4 *__restrict__ out, int64_t nvec, int64_t cvec)
+{
+    const int64_t S = (int64_t)gridDim.x * kThreads;
+    int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const bool fixed_col = S % cvec == 0;
+    const uint4 *bsrc = reinterpret_cast<const uint4 *>(b);
+    float m[8] = {}, ad[8] = {};
+    if constexpr (has_column_params(OP)) column_params<OP>(b, p0, p1, i % cvec, m, ad);
+    for (; i + 3 * S < nvec; i += 4 * S) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = ld_stream(a + i + u * S);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (has_column_params(OP) && !fixed_col) column_params<OP>(b, p0, p1, (i + u * S) % cvec, m, ad);
+            st_stream(out + i + u * S, chain_op<OP>(v[u], bsrc, i + u * S, m, ad));
+        }
+    }
+    for (; i < nvec; i += S) {
+        if (has_column_params(OP) && !fixed_col) column_params<OP>(b, p0, p1, i % cvec, m, ad);
+        st_stream(out + i, chain_op<OP>(ld_stream(a + i), bsrc, i, m, ad));
+    }
+}
+
+// One wave of resident CTAs, the stride a multiple of cvec when possible.
+template <Op OP>
+cudaError_t launch_chain(const void *a, const void *b, const float *p0, const float *p1, void *out, int64_t n,
                          int64_t cols, cudaStream_t st)
 {
-    const int64_t nvec = n / 8;
-    const unsigned grid = grid_for(reinterpret_cast<const void *>(chain_kernel<OP>), nvec);
-    chain_kernel<OP><<<grid, kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(a), b, scale,
-                                                 reinterpret_cast<uint4 *>(out), nvec, cols / 8);
+    const int64_t nvec = n / 8, cvec = cols / 8;
+    int64_t grid = grid_for(reinterpret_cast<const void *>(chain_kernel<OP>), nvec);
+    int64_t x = cvec, y = kThreads;
+    while (y) { const int64_t t = x % y; x = y; y = t; }   // gcd(cvec, threads)
+    const int64_t unit = cvec / x;
+    if (grid >= unit) grid = grid / unit * unit;
+    chain_kernel<OP><<<(unsigned)grid, kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(a), b, p0, p1,
+                                                           reinterpret_cast<uint4 *>(out), nvec, cvec);
     return cudaGetLastError();
 }
 
@@ -243,29 +291,35 @@ cudaError_t launch_bias_gelu(const void *x, const void *bias, void *y, int64_t r
 cudaError_t launch_unfused_bias_add(const void *x, const void *bias, void *t, int64_t rows,
                                     int64_t cols, cudaStream_t st)
 {
-    return launch_chain<Op::BiasAddF16>(x, bias, nullptr, t, rows * cols, cols, st);
+    return launch_chain<Op::BiasAddF16>(x, bias, nullptr, nullptr, t, rows * cols, cols, st);
 }
 
 cudaError_t launch_unfused_gelu(const void *t, void *y, int64_t n, cudaStream_t st)
 {
-    return launch_chain<Op::GeluF16>(t, nullptr, nullptr, y, n, 8, st);
+    return launch_chain<Op::GeluF16>(t, nullptr, nullptr, nullptr, y, n, 8, st);
 }
 
 cudaError_t launch_unfused_residual_add(const void *a, const void *r, void *s, int64_t n,
                                         cudaStream_t st)
 {
-    return launch_chain<Op::ResidualAddF16>(a, r, nullptr, s, n, 8, st);
+    return launch_chain<Op::ResidualAddF16>(a, r, nullptr, nullptr, s, n, 8, st);
 }
 
 cudaError_t launch_unfused_bn(const void *t1, const float *scale, const float *bias, void *t2,
                               int64_t M, int64_t C, cudaStream_t st)
 {
-    return launch_chain<Op::BnBf16>(t1, bias, scale, t2, M * C, C, st);
+    return launch_chain<Op::BnBf16>(t1, nullptr, scale, bias, t2, M * C, C, st);
 }
 
 cudaError_t launch_unfused_silu(const void *t2, void *y, int64_t n, cudaStream_t st)
 {
-    return launch_chain<Op::SiluBf16>(t2, nullptr, nullptr, y, n, 8, st);
+    return launch_chain<Op::SiluBf16>(t2, nullptr, nullptr, nullptr, y, n, 8, st);
+}
+
+cudaError_t launch_unfused_affine(const void *nrm, const float *gamma, const float *beta, void *y, int64_t rows,
+                                  int64_t hidden, cudaStream_t st)
+{
+    return launch_chain<Op::AffineF16>(nrm, nullptr, gamma, beta, y, rows * hidden, hidden, st);
 }
 
 cudaError_t launch_pack_filter(const void *w_oihw, void *w_ohwi, int C_out, int C_in, int KH, int KW,

@@ -1,5 +1,6 @@
 // Residual + LayerNorm + affine, fused into one pass over HBM, plus the
-// separate normalisation and scale-and-bias kernels of the unfused chain.
+// separate normalisation kernel of the unfused chain (its residual-add and
+// scale-and-bias kernels are the elementwise chain kernels).
 //
 // "Costs and benefits of kernel fusion", "Worked example: Fusing a residual
 // and normalization chain": load activation and residual once, compute the
@@ -426,29 +427,6 @@ __global__ void __launch_bounds__(1024) layernorm_cluster_kernel(const __half *_
     }
 }
 
-// y[i][j] = nrm[i][j] * gamma[j] + beta[j] (the unfused chain's last kernel).
-__global__ void __launch_bounds__(256) affine_kernel(const uint4 *__restrict__ nrm,
-                                                     const float *__restrict__ gamma,
-                                                     const float *__restrict__ beta,
-                                                     uint4 *__restrict__ y, int64_t nvec, int64_t cvec)
-{
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-        const uint4 v = ld_stream(nrm + i);
-        const int64_t c0 = (i % cvec) * 8;
-        const __half2 *h = reinterpret_cast<const __half2 *>(&v);
-        uint4 out;
-        __half2 *oh = reinterpret_cast<__half2 *>(&out);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 t = __half22float2(h[j]);
-            oh[j] = __floats2half2_rn(t.x * __ldg(gamma + c0 + 2 * j) + __ldg(beta + c0 + 2 * j),
-                                      t.y * __ldg(gamma + c0 + 2 * j + 1) + __ldg(beta + c0 + 2 * j + 1));
-        }
-        st_stream(y + i, out);
-    }
-}
-
 // Threads per row for NV vectors per thread: a whole number of warps.
 int threads_for(int64_t hidden, int nv)
 {
@@ -571,18 +549,6 @@ cudaError_t launch_unfused_layernorm(const void *s, void *nrm, int64_t rows, int
                                      cudaStream_t st)
 {
     return launch_ln<false, false>(s, nullptr, nullptr, nullptr, nrm, rows, hidden, eps, TF_LN_AUTO, st);
-}
-
-cudaError_t launch_unfused_affine(const void *nrm, const float *gamma, const float *beta, void *y,
-                                  int64_t rows, int64_t hidden, cudaStream_t st)
-{
-    const int64_t nvec = rows * hidden / 8;
-    int64_t g = (nvec + 255) / 256;
-    const int64_t cap = (int64_t)sm_count() * 8;
-    if (g > cap) g = cap;
-    affine_kernel<<<(unsigned)g, 256, 0, st>>>(reinterpret_cast<const uint4 *>(nrm), gamma, beta,
-                                               reinterpret_cast<uint4 *>(y), nvec, hidden / 8);
-    return cudaGetLastError();
 }
 
 }  // namespace tf
