@@ -371,6 +371,26 @@ def time_loop(fn, steps: int, warmup: int, world: int, clocks=None):
     return max_over_ranks(ms, world), launches
 
 
+def graph_time_us(fn, calls: int) -> float:
+    """GPU time per call with `calls` calls captured in one CUDA graph and
+    replayed, so the host's per-call launch cost is not counted."""
+    import torch
+    fn(0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        for i in range(calls):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / calls
+
+
 class _Null:
     def __enter__(self):
         return self
@@ -524,6 +544,8 @@ def main():
                 entry["fused"]["tflops"] = r.flops / (f_ms * 1e-3) / 1e12
             if name.startswith("conv3x3_tiny"):
                 entry["note"] = "launch-latency bound (0.59 MFLOP); reported as latency"
+                entry["fused"]["graph_us_per_call"] = graph_time_us(r.fused, 200)
+                entry["unfused_chain"]["graph_us_per_call"] = graph_time_us(r.unfused, 200)
             else:
                 entry["roofline"] = roofline("hbm", gbs, peaks["hbm_gbs"], "GB/s", kernel_traffic(name))
             workloads[name] = entry
