@@ -443,15 +443,14 @@ bool conv_umma_supports(const tf_conv_shape &s, int Ho, int Wo)
     if (s.C_in % BK != 0 || pick_bn(s.C_out) == 0) return false;
     if ((int64_t)s.N * Ho * Wo >= (int64_t)1 << 31) return false;
     if (is_plain_gemm(s)) return true;
-    // im2col geometry: this build takes symmetric geometry only (equal kernel
-    // extent, stride and padding along H and W), so the two spatial entries of
-    // the bounding-box corners are equal.
-    if (s.KH != s.KW || s.stride_h != s.stride_w || s.pad_h != s.pad_w) return false;
-    if (s.stride_w > 8 || s.KW > 256) return false;
+    // im2col geometry: traversal strides up to 8, filter taps addressed by
+    // 16-bit offsets, and bounding-box corners within the signed 8-bit range a
+    // 4-D im2col tensor map takes.
+    if (s.stride_h > 8 || s.stride_w > 8 || s.KH > 65535 || s.KW > 65535) return false;
     const int lw = -s.pad_w, uw = upper_corner(s.W, Wo, s.stride_w, s.pad_w);
     const int lh = -s.pad_h, uh = upper_corner(s.H, Ho, s.stride_h, s.pad_h);
-    if (lw != lh || uw != uh) return false;
-    if (lw < -128 || lw > 127 || uw < -128 || uw > 127) return false;
+    for (int c : {lw, uw, lh, uh})
+        if (c < -128 || c > 127) return false;
     return true;
 }
 

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) bias_gelu_kernel(const uint4 *__rest
 
 enum class Op { BiasAddF16, GeluF16, ResidualAddF16, BnBf16, SiluBf16, AffineF16 };
 
-constexpr bool has_column_params(Op op) { return op == Op::BiasAddF16 || op == Op::BnBf16 || op == Op::AffineF16; }
+__host__ __device__ constexpr bool has_column_params(Op op) { return op == Op::BiasAddF16 || op == Op::BnBf16 || op == Op::AffineF16; }
 
 // Per-column parameters of one 16-byte vector (columns c0 .. c0+7): the fp16
 // bias (BiasAddF16), or the fp32 scale/gamma and bias/beta pairs.

@@ -115,9 +115,8 @@ int tf_conv2d_bn_silu(const void *x, const void *w_ohwi, const float *scale, con
 
 /* Same as tf_conv2d_bn_silu with the kernel forced (TF_CONV_*).  Returns
  * TF_ERR_UNSUPPORTED when the forced kernel cannot take the shape
- * (TF_CONV_UMMA and TF_CONV_UMMA_PAIR need C_in % 64 == 0, C_out % 32 == 0, and either a 1x1
- * stride-1 unpadded filter or equal kernel extent, stride and padding along
- * H and W with padding <= 128 and stride <= 8). */
+ * (TF_CONV_UMMA and TF_CONV_UMMA_PAIR need C_in % 64 == 0, C_out % 32 == 0,
+ * strides <= 8 and padding <= 128). */
 int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *scale,
                               const float *bias, void *y, const tf_conv_shape *shape,
                               int variant, tf_stream_t stream);

@@ -105,6 +105,12 @@ UMMA_SHAPES = [
     synth.ConvShape(2, 10, 14, 128, 96, 3, 3, (1, 1), (1, 1)),      # non-square image, BN=32, 3 N tiles
     synth.ConvShape(1, 17, 17, 64, 64, 3, 3, (2, 2), (1, 1)),       # stride 2
     synth.ConvShape(1, 9, 9, 192, 512, 3, 3, (1, 1), (0, 0)),       # no padding, 2 N tiles of 256
+    synth.ConvShape(1, 12, 15, 64, 64, 3, 5, (1, 1), (1, 2)),       # non-square kernel and padding
+    synth.ConvShape(2, 10, 10, 64, 64, 1, 7, (1, 1), (0, 3)),       # 1x7
+    synth.ConvShape(1, 14, 9, 64, 32, 7, 1, (1, 1), (3, 0)),        # 7x1
+    synth.ConvShape(1, 16, 17, 64, 64, 3, 3, (2, 1), (1, 1)),       # different strides along H and W
+    synth.ConvShape(1, 17, 16, 64, 64, 3, 3, (2, 2), (1, 1)),       # stride 2 on odd and even extents
+    synth.ConvShape(1, 12, 12, 64, 64, 3, 3, (1, 1), (0, 1)),       # padding along W only
 ]
 
 
