@@ -92,12 +92,14 @@ __device__ __forceinline__ float ex2_approx(float x)
 // generated and checked by gen_gelu_poly.py); Phi(s) = 1 - Q(s) for s >= 0
 // and Q(-s) for s < 0, so the negative tail keeps its relative accuracy
 // without the cancellation of 1 + erf.  With w = s*Q(|s|) that is s - w for
-// s >= 0 and w for s < 0, which is max(s - w, w) since Q <= 1/2.  Beyond |s| = 6 the tail is clamped:
-// |s| * Q(6) is below half the smallest fp16 subnormal.  Cost: 9 FMA-pipe
-// operations and one ex2 per value.
+// s >= 0 and w for s < 0, which is max(s - w, w) since Q <= 1/2.  |s| is
+// clamped at 12: past the fit range the polynomial keeps falling (below
+// 2^-29 from |s| = 6, 2^-111 at 12), so |s*Q| rounds to zero in fp16 for every
+// |s| > 6, as the exact value does.  Cost: 9 FMA-pipe operations and one ex2
+// per value.
 __device__ __forceinline__ float gelu_f32(float s)
 {
-    const float t = fminf(fabsf(s), TF_GELU_TMAX);
+    const float t = fminf(fabsf(s), TF_GELU_TCLAMP);
     const float v = fmaf(t, 1.0f / (TF_GELU_TMAX * 0.5f), -1.0f);
     float acc = TF_GELU_C7;
     acc = fmaf(acc, v, TF_GELU_C6);
@@ -160,7 +162,7 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b)
 // (Q <= 1/2), so the sign test becomes a max.
 __device__ __forceinline__ float2 gelu_f32x2(float2 s)
 {
-    const float2 t = make_float2(fminf(fabsf(s.x), TF_GELU_TMAX), fminf(fabsf(s.y), TF_GELU_TMAX));
+    const float2 t = make_float2(fminf(fabsf(s.x), TF_GELU_TCLAMP), fminf(fabsf(s.y), TF_GELU_TCLAMP));
     const float k = 1.0f / (TF_GELU_TMAX * 0.5f);
     const float2 v = ffma2(t, make_float2(k, k), make_float2(-1.0f, -1.0f));
     float2 acc = ffma2(make_float2(TF_GELU_C7, TF_GELU_C7), v, make_float2(TF_GELU_C6, TF_GELU_C6));

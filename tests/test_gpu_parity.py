@@ -111,6 +111,8 @@ UMMA_SHAPES = [
     synth.ConvShape(1, 16, 17, 64, 64, 3, 3, (2, 1), (1, 1)),       # different strides along H and W
     synth.ConvShape(1, 17, 16, 64, 64, 3, 3, (2, 2), (1, 1)),       # stride 2 on odd and even extents
     synth.ConvShape(1, 12, 12, 64, 64, 3, 3, (1, 1), (0, 1)),       # padding along W only
+    synth.ConvShape(4, 7, 7, 64, 64, 7, 7, (1, 1), (0, 0)),         # 1x1 output: every tap interior
+    synth.ConvShape(1, 3, 3, 64, 64, 3, 3, (1, 1), (1, 1)),         # most taps in the padding
 ]
 
 
@@ -231,11 +233,11 @@ def test_bias_gelu(b, rows, cols):
     assert ulp.max() <= 2, f"max {ulp.max()} ulp"
 
 
-def test_bias_gelu_negative_tail(b):
-    # s from -10 to 10 on every fp16 value, bias zero: covers the fp16
-    # subnormal outputs of the deep negative tail
+def test_bias_gelu_every_fp16_input(b):
+    # every finite fp16 value of s, bias zero: the fp16 subnormal outputs of
+    # the deep negative tail, +-0, and the largest magnitudes (+-65504)
     xs = np.arange(0, 65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
-    xs = xs[np.isfinite(xs) & (np.abs(xs.astype(np.float32)) <= 10.0)]
+    xs = xs[np.isfinite(xs)]
     xs = xs[: (xs.size // 8) * 8].reshape(-1, 8)
     y = torch.empty(xs.shape, dtype=torch.float16, device="cuda")
     b.tf_bias_gelu(dev_f16(xs), dev_f16(np.zeros(8, np.float16)), y, xs.shape[0], 8)
@@ -283,6 +285,24 @@ def test_bias_gelu_rowsum_split(b, rows, cols):
     _rowsum_check(rs.cpu().numpy(), ref_y)
 
 
+def test_bias_gelu_beyond_2_to_31_elements(b):
+    # 262144 x 8200 = 2.15e9 values (64-bit indexing; 8200 / 8 = 1025 vectors
+    # per row, so the grid stride is not a multiple of the row and each vector
+    # reloads its bias).  The rows repeat a seeded 4096-row block on the device.
+    rows, cols, block = 262144, 8200, 4096
+    d = synth.bias_gelu_inputs(block, cols, seed=16)
+    x = dev_f16(d["x"]).repeat(rows // block, 1)
+    y = torch.empty((rows, cols), dtype=torch.float16, device="cuda")
+    b.tf_bias_gelu(x, dev_f16(d["bias"]), y, rows, cols)
+    torch.cuda.synchronize()
+    del x
+    ref = oracle.bias_gelu(d["x"], d["bias"])
+    for r in (0, 1, block - 1, 131071, 200003, rows - 1):
+        ulp = f16_ulp_distance(y[r].cpu().numpy().view(np.uint16), ref[r % block])
+        assert ulp.max() <= 2, (r, ulp.max())
+    _assert_no_device_error(b)
+
+
 # ---------------------------------------------------------------- residual + LayerNorm
 
 @pytest.mark.parametrize("rows,hidden", [(1, 8), (5, 200), (33, 4096), (7, 16384), (16384, 4096)])
@@ -324,6 +344,22 @@ def test_layernorm_wide_rows_dispatch(b):
     torch.cuda.synchronize()
     ref = oracle.residual_layernorm(d["act"], d["res"], d["gamma"], d["beta"], eps=1e-5)
     assert np.abs(y.cpu().numpy().astype(np.float64) - ref).max() <= 1e-2
+
+
+def test_layernorm_beyond_2_to_31_elements(b):
+    # 262144 x 8200 = 2.15e9 values per tensor, rows repeating a seeded block
+    rows, hidden, block = 262144, 8200, 2048
+    d = synth.layernorm_inputs(block, hidden, seed=17)
+    act = dev_f16(d["act"]).repeat(rows // block, 1)
+    res = dev_f16(d["res"]).repeat(rows // block, 1)
+    y = torch.empty((rows, hidden), dtype=torch.float16, device="cuda")
+    b.tf_residual_layernorm(act, res, dev_f32(d["gamma"]), dev_f32(d["beta"]), y, rows, hidden, 1e-5)
+    torch.cuda.synchronize()
+    del act, res
+    ref = oracle.residual_layernorm(d["act"], d["res"], d["gamma"], d["beta"], eps=1e-5)
+    for r in (0, block - 1, 131071, 200003, rows - 1):
+        assert np.abs(y[r].cpu().numpy().astype(np.float64) - ref[r % block]).max() <= 1e-2, r
+    _assert_no_device_error(b)
 
 
 def test_layernorm_constant_row(b):
