@@ -5,13 +5,12 @@
 // bias, GELU and a per-row reduction in one pass; the split path writes the
 // GELU result first and then runs the reduction over it.
 //
-// Both kernels work on tiles of kRows rows.  A persistent CTA of 256 threads
+// Both kernels work on tiles of a few rows.  A persistent CTA of 256 threads
 // walks the tiles blockIdx.x, +gridDim.x, ...; thread t owns the 16-byte
 // column vectors t, t+256, ... of every row and keeps one fp32 partial sum
-// per row of the tile.  For each of its columns the kRows loads of the tile
-// (independent 16-byte loads) are in flight together.  At the end of a tile the CTA
-// reduces the kRows partial sums at once (warp shuffles, one shared-memory
-// step): one pair of barriers per kRows rows.  The fused kernel sums the fp32
+// per row of the tile; all of its loads of a tile are in flight together.
+// At the end of a tile the CTA reduces the tile's partial sums at once (warp
+// shuffles, one shared-memory step): one pair of barriers per tile.  The fused kernel sums the fp32
 // GELU values before rounding y to fp16; the split path's reduction sums the
 // stored fp16 values.
 #include <cuda_fp16.h>
@@ -22,7 +21,6 @@ namespace tf {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRows = 8;      // rows per tile
 constexpr int kMaxChunks = 8; // column vectors per thread: cols <= 8 * 256 * 8 = 16384
 
 __device__ __forceinline__ uint4 ld_stream(const void *p)
@@ -41,31 +39,42 @@ __device__ __forceinline__ void st_stream(void *p, uint4 v)
 
 // FUSED: x, bias -> y = GELU(x + bias) (fp16) and rowsum (fp32).
 // !FUSED: x is the stored GELU result; only rowsum is written.
-template <bool FUSED>
-__global__ void __launch_bounds__(kThreads, 4) rowsum_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ bias,
-                                                          uint4 *__restrict__ y, float *__restrict__ rowsum,
-                                                          int64_t rows, int cvec)
+// A tile is R rows; a thread owns the column vectors t + 256k, k < C, of each
+// of them (C = ceil(cvec / 256)), so R * C = 8 independent 16-byte loads are in
+// flight per thread, and small R keeps the tiles fine-grained enough to spread
+// evenly over the persistent CTAs.
+template <bool FUSED, int R, int C>
+__global__ void __launch_bounds__(kThreads, 4) rowsum_kernel(const uint4 *__restrict__ x,
+                                                             const uint4 *__restrict__ bias,
+                                                             uint4 *__restrict__ y, float *__restrict__ rowsum,
+                                                             int64_t rows, int cvec)
 {
-    __shared__ float red[kThreads / 32][kRows];
+    __shared__ float red[kThreads / 32][R];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t ntiles = (rows + kRows - 1) / kRows;
+    const int64_t ntiles = (rows + R - 1) / R;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const int64_t r0 = tile * kRows;
-        float sum[kRows];
+        const int64_t r0 = tile * R;
+        uint4 xv[R][C];
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) sum[r] = 0.0f;
-#pragma unroll 1
-        for (int v = threadIdx.x; v < cvec; v += kThreads) {
-            uint4 xv[kRows];
+        for (int k = 0; k < C; ++k) {
+            const int v = threadIdx.x + k * kThreads;
 #pragma unroll
-            for (int r = 0; r < kRows; ++r)
-                xv[r] = r0 + r < rows ? ld_stream(x + (r0 + r) * cvec + v) : make_uint4(0, 0, 0, 0);
+            for (int r = 0; r < R; ++r)
+                xv[r][k] = (v < cvec && r0 + r < rows) ? ld_stream(x + (r0 + r) * cvec + v) : make_uint4(0, 0, 0, 0);
+        }
+        float sum[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) sum[r] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < C; ++k) {
+            const int v = threadIdx.x + k * kThreads;
+            if (v >= cvec) continue;
             uint4 braw = make_uint4(0, 0, 0, 0);
-            if (FUSED) braw = __ldg(bias + v);   // 16 KB of bias: an L1 hit after the first tile
+            if (FUSED) braw = __ldg(bias + v);   // 16 KB of bias: L1 hits after the first tile
             const __half2 *bh = reinterpret_cast<const __half2 *>(&braw);
 #pragma unroll
-            for (int r = 0; r < kRows; ++r) {
-                const __half2 *h = reinterpret_cast<const __half2 *>(&xv[r]);
+            for (int r = 0; r < R; ++r) {
+                const __half2 *h = reinterpret_cast<const __half2 *>(&xv[r][k]);
                 if (FUSED) {
                     uint4 o;
                     __half2 *oh = reinterpret_cast<__half2 *>(&o);
@@ -85,19 +94,19 @@ __global__ void __launch_bounds__(kThreads, 4) rowsum_kernel(const uint4 *__rest
                 }
             }
         }
-        // the tile's kRows sums: shuffle within each warp, then across warps
+        // the tile's R sums: shuffle within each warp, then across warps
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
+        for (int r = 0; r < R; ++r) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], o);
         }
         __syncthreads();   // `red` of the previous tile has been read
         if (lane == 0) {
 #pragma unroll
-            for (int r = 0; r < kRows; ++r) red[warp][r] = sum[r];
+            for (int r = 0; r < R; ++r) red[warp][r] = sum[r];
         }
         __syncthreads();
-        if (threadIdx.x < kRows && r0 + threadIdx.x < rows) {
+        if (threadIdx.x < R && r0 + threadIdx.x < rows) {
             float t = 0.0f;
 #pragma unroll
             for (int w = 0; w < kThreads / 32; ++w) t += red[w][threadIdx.x];
@@ -112,17 +121,23 @@ cudaError_t launch_rowsum(const void *x, const void *bias, void *y, float *rowsu
 {
     const int64_t cvec = cols / 8;
     if (cvec > (int64_t)kThreads * kMaxChunks) return cudaErrorNotSupported;
-    const int64_t ntiles = (rows + kRows - 1) / kRows;
-    auto kern = rowsum_kernel<FUSED>;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm < 1)
-        per_sm = 1;
-    int64_t grid = (int64_t)sm_count() * per_sm;
-    if (grid > ntiles) grid = ntiles;
-    kern<<<(unsigned)grid, kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(x),
-                                              reinterpret_cast<const uint4 *>(bias), reinterpret_cast<uint4 *>(y),
-                                              rowsum, rows, (int)cvec);
-    return cudaGetLastError();
+    auto go = [&](auto kern, int R) -> cudaError_t {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm < 1)
+            per_sm = 1;
+        const int64_t ntiles = (rows + R - 1) / R;
+        int64_t grid = (int64_t)sm_count() * per_sm;
+        if (grid > ntiles) grid = ntiles;
+        kern<<<(unsigned)grid, kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(x),
+                                                  reinterpret_cast<const uint4 *>(bias),
+                                                  reinterpret_cast<uint4 *>(y), rowsum, rows, (int)cvec);
+        return cudaGetLastError();
+    };
+    const int64_t chunks = (cvec + kThreads - 1) / kThreads;
+    if (chunks <= 1) return go(rowsum_kernel<FUSED, 8, 1>, 8);
+    if (chunks <= 2) return go(rowsum_kernel<FUSED, 4, 2>, 4);
+    if (chunks <= 4) return go(rowsum_kernel<FUSED, 2, 4>, 2);
+    return go(rowsum_kernel<FUSED, 1, 8>, 1);
 }
 
 }  // namespace
