@@ -328,103 +328,164 @@ __device__ __forceinline__ float cta_sum(float v, float *red)
 }
 
 // Wide rows (hidden > 16384): a thread-block cluster owns a row; CTA r of the
-// cluster holds the slice [r*slice, (r+1)*slice) in registers (2 vectors per
-// thread).  Each reduction is a CTA sum followed by an exchange of the
-// per-CTA partials through distributed shared memory, so the row is still
-// read from HBM exactly once ("a hidden width large enough to require a
-// different row-reduction strategy").
+// cluster owns the slice [r*slice, (r+1)*slice).  Clusters are persistent and
+// walk the rows c, c + nclusters, ...; like the CTA-per-row kernel, thread 0
+// of every CTA streams its slice of the coming rows (act and res) into a
+// shared-memory ring with bulk copies, and each thread holds 2 vectors of the
+// current row in fp32 registers.  Each reduction is a CTA sum followed by an
+// exchange of the per-CTA partials through distributed shared memory, so a
+// row is still read from HBM exactly once ("a hidden width large enough to
+// require a different row-reduction strategy").  The partials are
+// double-buffered by row parity: two cluster barriers per row suffice.
 template <bool RESIDUAL, bool AFFINE>
-__global__ void __launch_bounds__(1024) layernorm_cluster_kernel(const __half *__restrict__ a,
+__global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half *__restrict__ a,
                                                                  const __half *__restrict__ b,
                                                                  const float *__restrict__ gamma,
                                                                  const float *__restrict__ beta,
-                                                                 __half *__restrict__ y, int hidden, int slice,
-                                                                 float eps)
+                                                                 __half *__restrict__ y, int64_t rows, int hidden,
+                                                                 int slice, float eps, int stages, uint32_t *err,
+                                                                 uint64_t wait_ns)
 {
     constexpr int NV = 2;
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[32];
-    __shared__ float part[2];
+    __shared__ float part[2][2];
     const uint32_t rank = ptx::cluster_ctarank(), nranks = cluster_nctarank();
-    const int64_t row = blockIdx.x / nranks;
+    const int64_t cid = blockIdx.x / nranks, ncl = gridDim.x / nranks;
     const int c0 = (int)rank * slice;                    // first column of this CTA's slice
-    const int nvec = (min(hidden - c0, slice)) >> 3;     // vectors in the slice
-    const __half *ar = a + row * hidden + c0;
-    const __half *br = RESIDUAL ? b + row * hidden + c0 : nullptr;
+    const int width = min(hidden - c0, slice);           // columns in the slice (a multiple of 8)
+    const int nvec = width >> 3;
+    const uint32_t part_bytes = (uint32_t)width * 2u;
+    const uint32_t stage_bytes = (uint32_t)slice * 2u * (RESIDUAL ? 2u : 1u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stage_bytes);
 
-    float s[NV][8];
-    float sum = 0.0f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int v = threadIdx.x + k * blockDim.x;
-        uint4 av = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
-        if (v < nvec) {
-            av = ld_stream(ar + 8 * v);
-            if (RESIDUAL) bv = ld_stream(br + 8 * v);
-        }
-        const __half2 *ah = reinterpret_cast<const __half2 *>(&av);
-        const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float2 t = __half22float2(ah[j]);
-            if (RESIDUAL) {
-                const float2 u = __half22float2(bh[j]);
-                t.x += u.x;
-                t.y += u.y;
-            }
-            s[k][2 * j] = t.x;
-            s[k][2 * j + 1] = t.y;
-            sum += t.x + t.y;
+    auto issue = [&](int st, int64_t row) {
+        unsigned char *dst = smem + (size_t)st * stage_bytes;
+        ptx::mbar_arrive_expect_tx(&full[st], RESIDUAL ? 2u * part_bytes : part_bytes);
+        ptx::bulk_load(dst, a + row * hidden + c0, part_bytes, &full[st]);
+        if (RESIDUAL) ptx::bulk_load(dst + (size_t)slice * 2, b + row * hidden + c0, part_bytes, &full[st]);
+    };
+    // (the launcher gives every CTA of the cluster at least 8 columns)
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < stages; ++st) ptx::mbar_init(&full[st], 1);
+        ptx::mbar_init_fence();
+        for (int st = 0; st < stages; ++st) {
+            const int64_t row = cid + st * ncl;
+            if (row >= rows) break;
+            issue(st, row);
         }
     }
+    __syncthreads();
+
     const float inv_h = 1.0f / (float)hidden;
-    float total = cta_sum(sum, red);
-    if (threadIdx.x == 0) part[0] = total;
-    ptx::cluster_sync();
-    total = 0.0f;
-    for (uint32_t r = 0; r < nranks; ++r) total += ld_dsmem(&part[0], r);
-    const float mean = total * inv_h;
-    float sq = 0.0f;
+    // After a time-out this CTA stops waiting and stops issuing copies but
+    // still runs every row, so its cluster barriers stay matched with its
+    // peers' (the results are void; the error word says so).
+    bool failed = false;
+    int fail_it = 0;                     // the first row whose copy timed out
+    int issued_until = stages;           // this CTA's rows 0 .. issued_until-1 had copies issued
+    int it = 0;
+    for (int64_t row = cid; row < rows; row += ncl, ++it) {
+        const int st = it % stages;
+        const int pb = it & 1;
+        const bool ok = !failed && ptx::mbar_wait(&full[st], (uint32_t)(it / stages) & 1u, wait_ns);
+        if (!__syncthreads_and(ok) && !failed) {
+            failed = true;
+            fail_it = it;
+            if (threadIdx.x == 0) atomicOr(err, TF_DEVERR_PRODUCER_WAIT);
+        }
+        const unsigned char *src = smem + (size_t)st * stage_bytes;
+        float s[NV][8];
+        float sum = 0.0f;
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        if (threadIdx.x + k * blockDim.x < nvec) {
+        for (int k = 0; k < NV; ++k) {
+            const int v = threadIdx.x + k * blockDim.x;
+            uint4 av = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
+            if (v < nvec) {
+                av = reinterpret_cast<const uint4 *>(src)[v];
+                if (RESIDUAL) bv = reinterpret_cast<const uint4 *>(src + (size_t)slice * 2)[v];
+            }
+            const __half2 *ah = reinterpret_cast<const __half2 *>(&av);
+            const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float d = s[k][j] - mean;
-                sq = fmaf(d, d, sq);
+            for (int j = 0; j < 4; ++j) {
+                float2 t = __half22float2(ah[j]);
+                if (RESIDUAL) {
+                    const float2 u = __half22float2(bh[j]);
+                    t.x += u.x;
+                    t.y += u.y;
+                }
+                s[k][2 * j] = t.x;
+                s[k][2 * j + 1] = t.y;
+                sum += t.x + t.y;
             }
         }
+        float total = cta_sum(sum, red);
+        if (threadIdx.x == 0) {
+            part[pb][0] = total;
+            // every thread has read stage `st`: refill it with the row `stages` ahead
+            const int64_t next = row + (int64_t)stages * ncl;
+            if (next < rows && !failed) {
+                ptx::fence_proxy_async_smem();
+                issue(st, next);
+                issued_until = it + stages + 1;
+            }
+        }
+        ptx::cluster_sync();
+        total = 0.0f;
+        for (uint32_t r = 0; r < nranks; ++r) total += ld_dsmem(&part[pb][0], r);
+        const float mean = total * inv_h;
+        float sq = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            if (threadIdx.x + k * blockDim.x < nvec) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float d = s[k][j] - mean;
+                    sq = fmaf(d, d, sq);
+                }
+            }
+        }
+        float sqt = cta_sum(sq, red);
+        if (threadIdx.x == 0) part[pb][1] = sqt;
+        ptx::cluster_sync();
+        sqt = 0.0f;
+        for (uint32_t r = 0; r < nranks; ++r) sqt += ld_dsmem(&part[pb][1], r);
+        const float rstd = rsqrtf(sqt * inv_h + eps);
+        __half *yr = y + row * hidden + c0;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int v = threadIdx.x + k * blockDim.x;
+            if (v >= nvec) continue;
+            float g[8], bb[8];
+            if (AFFINE) {
+                const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gamma + c0 + 8 * v));
+                const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gamma + c0 + 8 * v + 4));
+                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + c0 + 8 * v));
+                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + c0 + 8 * v + 4));
+                g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w; g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+                bb[0] = b0.x; bb[1] = b0.y; bb[2] = b0.z; bb[3] = b0.w; bb[4] = b1.x; bb[5] = b1.y; bb[6] = b1.z; bb[7] = b1.w;
+            }
+            uint4 out;
+            __half2 *oh = reinterpret_cast<__half2 *>(&out);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float o0 = (s[k][2 * j] - mean) * rstd, o1 = (s[k][2 * j + 1] - mean) * rstd;
+                oh[j] = AFFINE ? __floats2half2_rn(fmaf(o0, g[2 * j], bb[2 * j]), fmaf(o1, g[2 * j + 1], bb[2 * j + 1]))
+                               : __floats2half2_rn(o0, o1);
+            }
+            st_stream(yr + 8 * v, out);
+        }
     }
-    float sqt = cta_sum(sq, red);
-    if (threadIdx.x == 0) part[1] = sqt;
-    ptx::cluster_sync();
-    sqt = 0.0f;
-    for (uint32_t r = 0; r < nranks; ++r) sqt += ld_dsmem(&part[1], r);
+    if (threadIdx.x == 0 && failed) {   // copies issued but never consumed land before exit
+        for (int k = fail_it; k < issued_until; ++k) {
+            const int64_t row = cid + (int64_t)k * ncl;
+            if (row >= rows) break;
+            if (!ptx::mbar_wait(&full[k % stages], (uint32_t)(k / stages) & 1u, wait_ns))
+                atomicOr(err, TF_DEVERR_DRAIN_WAIT);
+        }
+    }
     ptx::cluster_sync();   // no CTA leaves while another may still read its `part`
-    const float rstd = rsqrtf(sqt * inv_h + eps);
-    __half *yr = y + row * hidden + c0;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int v = threadIdx.x + k * blockDim.x;
-        if (v >= nvec) continue;
-        float g[8], bb[8];
-        if (AFFINE) {
-            const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gamma + c0 + 8 * v));
-            const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gamma + c0 + 8 * v + 4));
-            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + c0 + 8 * v));
-            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + c0 + 8 * v + 4));
-            g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w; g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
-            bb[0] = b0.x; bb[1] = b0.y; bb[2] = b0.z; bb[3] = b0.w; bb[4] = b1.x; bb[5] = b1.y; bb[6] = b1.z; bb[7] = b1.w;
-        }
-        uint4 out;
-        __half2 *oh = reinterpret_cast<__half2 *>(&out);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float o0 = (s[k][2 * j] - mean) * rstd, o1 = (s[k][2 * j + 1] - mean) * rstd;
-            oh[j] = AFFINE ? __floats2half2_rn(fmaf(o0, g[2 * j], bb[2 * j]), fmaf(o1, g[2 * j + 1], bb[2 * j + 1]))
-                           : __floats2half2_rn(o0, o1);
-        }
-        st_stream(yr + 8 * v, out);
-    }
 }
 
 // Threads per row for NV vectors per thread: a whole number of warps.
@@ -490,29 +551,44 @@ cudaError_t launch_ln_cluster(const void *a, const void *b, const float *gamma, 
                               int64_t rows, int64_t hidden, float eps, cudaStream_t st)
 {
     if (hidden > kClusterMaxHidden) return cudaErrorNotSupported;
-    // Fewest CTAs per row (at most 8, the portable cluster size) with at
-    // most 1024 threads x 16 values each; the slice is a multiple of 8.
-    int csize = 1;
-    while ((int64_t)csize * 1024 * 16 < hidden) ++csize;
+    uint32_t *err = device_error_word();
+    if (!err) return cudaErrorInitializationError;
+    // Slices of at most 8192 values (so two CTAs fit an SM) while the cluster
+    // stays within the portable 8 CTAs; 16384 per CTA beyond 65536.
+    int csize = (int)((hidden + 8191) / 8192);
     if (csize < 2) csize = 2;
+    if (csize > 8) csize = 8;
+    while (csize > 1 && (csize - 1) * (((hidden + csize - 1) / csize + 7) / 8 * 8) >= hidden) --csize;  // no empty slice
     const int64_t slice = ((hidden + csize - 1) / csize + 7) / 8 * 8;
     const int threads = threads_for(slice, 2);
-    if (rows * csize > 0x7fffffff) return cudaErrorNotSupported;
+    const size_t stage_bytes = (size_t)slice * 2 * (RESIDUAL ? 2 : 1);
+    int stages = (int)((96 * 1024) / stage_bytes);
+    stages = stages < 2 ? 2 : (stages > 4 ? 4 : stages);
+    const size_t smem = (size_t)stages * stage_bytes + 8 * (size_t)stages;
+    auto kern = layernorm_cluster_kernel<RESIDUAL, AFFINE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(rows * csize));
-    cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, layernorm_cluster_kernel<RESIDUAL, AFFINE>, reinterpret_cast<const __half *>(a),
-                              reinterpret_cast<const __half *>(b), gamma, beta, reinterpret_cast<__half *>(y),
-                              (int)hidden, (int)slice, eps);
+    cfg.gridDim = dim3(sm_count() / csize * csize);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorNotSupported;
+    if (clusters > rows) clusters = (int)rows;
+    cfg.gridDim = dim3((unsigned)(clusters * csize));
+    return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const __half *>(a), reinterpret_cast<const __half *>(b),
+                              gamma, beta, reinterpret_cast<__half *>(y), rows, (int)hidden, (int)slice, eps, stages,
+                              err, wait_limit_ns());
 }
 
 template <bool RESIDUAL, bool AFFINE>
