@@ -302,16 +302,6 @@ __device__ __forceinline__ uint32_t cluster_nctarank()
     return r;
 }
 
-// Reads a float from the same shared-memory variable in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_dsmem(const float *local, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ptx::smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ float cta_sum(float v, float *red)
 {
 #pragma unroll
@@ -332,11 +322,16 @@ __device__ __forceinline__ float cta_sum(float v, float *red)
 // walk the rows c, c + nclusters, ...; like the CTA-per-row kernel, thread 0
 // of every CTA streams its slice of the coming rows (act and res) into a
 // shared-memory ring with bulk copies, and each thread holds 2 vectors of the
-// current row in fp32 registers.  Each reduction is a CTA sum followed by an
-// exchange of the per-CTA partials through distributed shared memory, so a
-// row is still read from HBM exactly once ("a hidden width large enough to
-// require a different row-reduction strategy").  The partials are
-// double-buffered by row parity: two cluster barriers per row suffice.
+// current row in fp32 registers, so a row is still read from HBM exactly once
+// ("a hidden width large enough to require a different row-reduction
+// strategy").  Each of the two reductions is a CTA sum followed by an
+// exchange: thread r pushes the CTA's partial into slot [rank] of CTA r with
+// st.async, which completes on CTA r's own mbarrier, and every CTA adds the
+// nranks slots in rank order (so all CTAs of the cluster get the same
+// value).  No cluster-wide barrier is taken per row.  Slots and mbarriers
+// are double-buffered by row parity: a peer can only be one row ahead, since
+// it cannot finish row i+1 without this CTA's second partial of row i+1,
+// which is sent after this CTA has read every slot of row i.
 template <bool RESIDUAL, bool AFFINE>
 __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half *__restrict__ a,
                                                                  const __half *__restrict__ b,
@@ -347,13 +342,15 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
                                                                  uint64_t wait_ns)
 {
     constexpr int NV = 2;
+    constexpr int kMaxRanks = 8;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[32];
-    __shared__ float part[2][2];
+    __shared__ float slot[2][2][kMaxRanks];   // [row parity][sum, squares][sending rank]
+    __shared__ __align__(8) uint64_t xbar[2][2];
     const uint32_t rank = ptx::cluster_ctarank(), nranks = cluster_nctarank();
     const int64_t cid = blockIdx.x / nranks, ncl = gridDim.x / nranks;
     const int c0 = (int)rank * slice;                    // first column of this CTA's slice
-    const int width = min(hidden - c0, slice);           // columns in the slice (a multiple of 8)
+    const int width = min(hidden - c0, slice);           // columns in the slice (a multiple of 8, >= 8)
     const int nvec = width >> 3;
     const uint32_t part_bytes = (uint32_t)width * 2u;
     const uint32_t stage_bytes = (uint32_t)slice * 2u * (RESIDUAL ? 2u : 1u);
@@ -365,9 +362,10 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
         ptx::bulk_load(dst, a + row * hidden + c0, part_bytes, &full[st]);
         if (RESIDUAL) ptx::bulk_load(dst + (size_t)slice * 2, b + row * hidden + c0, part_bytes, &full[st]);
     };
-    // (the launcher gives every CTA of the cluster at least 8 columns)
     if (threadIdx.x == 0) {
         for (int st = 0; st < stages; ++st) ptx::mbar_init(&full[st], 1);
+        for (int p = 0; p < 2; ++p)
+            for (int q = 0; q < 2; ++q) ptx::mbar_init(&xbar[p][q], 1);
         ptx::mbar_init_fence();
         for (int st = 0; st < stages; ++st) {
             const int64_t row = cid + st * ncl;
@@ -375,12 +373,30 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
             issue(st, row);
         }
     }
-    __syncthreads();
+    ptx::cluster_sync();   // every CTA's exchange barriers exist before the first push
+
+    // Sends this CTA's partial v (held by every thread) to slot[p][q][rank] of
+    // every CTA of the cluster; returns the rank-ordered sum of the nranks
+    // partials once they have all arrived here.
+    bool xfail = false;
+    auto exchange = [&](float v, int p, int q, uint32_t parity) -> float {
+        if (threadIdx.x == 0 && !xfail) ptx::mbar_arrive_expect_tx(&xbar[p][q], nranks * 4u);
+        if (threadIdx.x < nranks)
+            ptx::st_async_f32(ptx::mapa_shared(&slot[p][q][rank], threadIdx.x), v,
+                              ptx::mapa_shared(&xbar[p][q], threadIdx.x));
+        const bool ok = !xfail && ptx::mbar_wait<true>(&xbar[p][q], parity, wait_ns);
+        if (!ok && !xfail) {   // a peer stalled: stop using the barriers (results are void)
+            xfail = true;
+            atomicOr(err, TF_DEVERR_EXCHANGE_WAIT);
+        }
+        float t = 0.0f;
+        for (uint32_t r = 0; r < nranks; ++r) t += slot[p][q][r];
+        return t;
+    };
 
     const float inv_h = 1.0f / (float)hidden;
-    // After a time-out this CTA stops waiting and stops issuing copies but
-    // still runs every row, so its cluster barriers stay matched with its
-    // peers' (the results are void; the error word says so).
+    // After a copy time-out this CTA stops waiting for and issuing copies but
+    // still runs every row and every exchange, so its peers never wait on it.
     bool failed = false;
     int fail_it = 0;                     // the first row whose copy timed out
     int issued_until = stages;           // this CTA's rows 0 .. issued_until-1 had copies issued
@@ -388,6 +404,7 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
     for (int64_t row = cid; row < rows; row += ncl, ++it) {
         const int st = it % stages;
         const int pb = it & 1;
+        const uint32_t xpar = (uint32_t)(it >> 1) & 1u;
         const bool ok = !failed && ptx::mbar_wait(&full[st], (uint32_t)(it / stages) & 1u, wait_ns);
         if (!__syncthreads_and(ok) && !failed) {
             failed = true;
@@ -420,10 +437,8 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
                 sum += t.x + t.y;
             }
         }
-        float total = cta_sum(sum, red);
+        const float total = cta_sum(sum, red);   // its barriers also mean every thread has read stage `st`
         if (threadIdx.x == 0) {
-            part[pb][0] = total;
-            // every thread has read stage `st`: refill it with the row `stages` ahead
             const int64_t next = row + (int64_t)stages * ncl;
             if (next < rows && !failed) {
                 ptx::fence_proxy_async_smem();
@@ -431,10 +446,7 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
                 issued_until = it + stages + 1;
             }
         }
-        ptx::cluster_sync();
-        total = 0.0f;
-        for (uint32_t r = 0; r < nranks; ++r) total += ld_dsmem(&part[pb][0], r);
-        const float mean = total * inv_h;
+        const float mean = exchange(total, pb, 0, xpar) * inv_h;
         float sq = 0.0f;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -446,12 +458,7 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
                 }
             }
         }
-        float sqt = cta_sum(sq, red);
-        if (threadIdx.x == 0) part[pb][1] = sqt;
-        ptx::cluster_sync();
-        sqt = 0.0f;
-        for (uint32_t r = 0; r < nranks; ++r) sqt += ld_dsmem(&part[pb][1], r);
-        const float rstd = rsqrtf(sqt * inv_h + eps);
+        const float rstd = rsqrtf(exchange(cta_sum(sq, red), pb, 1, xpar) * inv_h + eps);
         __half *yr = y + row * hidden + c0;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -485,7 +492,7 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
                 atomicOr(err, TF_DEVERR_DRAIN_WAIT);
         }
     }
-    ptx::cluster_sync();   // no CTA leaves while another may still read its `part`
+    ptx::cluster_sync();   // no CTA leaves while a peer's push to it may be in flight
 }
 
 // Threads per row for NV vectors per thread: a whole number of warps.

@@ -276,6 +276,7 @@ uint64_t tf_get_wait_limit_ns(void);
 #define TF_DEVERR_EPILOGUE_WAIT 0x4u  /* epilogue: accumulator never committed */
 #define TF_DEVERR_DRAIN_WAIT 0x8u     /* in-flight copies/MMAs not drained on exit */
 #define TF_DEVERR_PROBE_WAIT 0x10u    /* tf_wait_probe: the expected time-out */
+#define TF_DEVERR_EXCHANGE_WAIT 0x20u /* cluster LayerNorm: a peer CTA's partial sum never arrived */
 
 /* Synchronises the current device, copies the device error word of the
  * current device into *word (may be NULL), clears it, and returns TF_OK if it
