@@ -34,26 +34,38 @@ namespace {
 constexpr int BM = 128;            // output pixels per tile (UMMA M)
 constexpr int BK = 64;             // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
-constexpr int kStages = 4;
+constexpr int kMaxStages = 6;      // deepest operand ring the shared-memory plan may choose
+constexpr int kSmemLimit = 227 * 1024;        // opt-in dynamic shared memory per block
+constexpr int kBResMaxBytes = 128 * 1024;     // largest filter block kept resident in shared memory
+constexpr int kParamChunkBytes = 64 * 4;      // 32 scale + 32 bias floats of one 32-channel chunk
 // Epilogue warps: 16 (four per TMEM lane quarter) for short K loops, where the
 // epilogue paces the kernel; 8 for long ones, where it hides behind the MMAs.
 constexpr int kEpiWarpsShortK = 16, kEpiWarpsLongK = 8;
 constexpr int threads_for(int epi_warps) { return 64 + 32 * epi_warps; }
+// 32-channel accumulator chunks each epilogue warp handles per tile
+constexpr int chunks_per_warp(int bn, int epi_warps) { return bn / 32 / (epi_warps / 4) > 0 ? bn / 32 / (epi_warps / 4) : 1; }
 constexpr int kOutBox = 32;        // epilogue store box: 32 pixels x 32 channels (64 B rows)
 constexpr int kOutBoxBytes = kOutBox * kOutBox * 2;
 
-template <int BN, int kEpiWarps>
-struct Layout {
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int OUT_OFFSET = kStages * STAGE_BYTES;                 // 1024-aligned
-    static constexpr int OUT_BYTES = kEpiWarps * kOutBoxBytes;               // one staging box per warp
-    static constexpr int BAR_OFFSET = OUT_OFFSET + OUT_BYTES;
-    static constexpr int NUM_BARS = 2 * kStages + 5;  // full, empty, tmem full x2, tmem empty x2, drain
-    static constexpr int TOTAL = BAR_OFFSET + NUM_BARS * 8 + 16;
-    static constexpr int ALLOC = TOTAL + 1024;        // slack to align the base to 1024 B
+constexpr int kABytes = BM * BK * 2;          // one A (im2col) tile of a K step
+constexpr int kNumBars = 2 * kMaxStages + 5;  // full, empty, tmem full x2, tmem empty x2, drain
+constexpr int kBarBytes = kNumBars * 8 + 16;  // + the TMEM address slot
+
+template <int BN>
+struct Tile {
+    static constexpr int B_BYTES = BN * BK * 2;   // one B (filter) tile of a K step
     static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+};
+
+// Shared-memory plan, from the 1024-byte-aligned base (operand tiles use
+// the 128-byte swizzle, whose atoms are 1024 B):
+//   [0, off_bres)          operand ring: `stages` x (A tile, + B tile unless resident)
+//   [off_bres, off_out)    resident filter block: num_kb B tiles (b_res only)
+//   [off_out, off_par)     one 2 KB output staging box per epilogue warp
+//   [off_par, off_bar)     per epilogue warp, the scale/bias values of its chunks
+//   [off_bar, total)       mbarriers and the TMEM address slot
+struct SmemPlan {
+    int stages, stage_bytes, b_res, off_bres, off_out, off_par, off_bar, alloc;
 };
 
 struct UmmaParams {
@@ -68,6 +80,7 @@ struct UmmaParams {
     int epilogue;            // 0: plain bf16 store, 1: BN + SiLU, 2: fp32 split-K partial to ws
     int splits, kb_per_split, num_work;   // work item = (tile, K split), split fastest
     float *ws;               // split-K partials [splits][M][C_out] (epilogue 2 only)
+    SmemPlan sm;
 };
 
 // CL: CTAs per cluster along M (1 or 2).  With CL = 2 the two CTAs of a
@@ -76,27 +89,39 @@ struct UmmaParams {
 // thread's stage release is multicast to both producers, so a stage is
 // refilled only after both CTAs have consumed it.  Every SM then fetches
 // 16 KB of A + BN*64 B of B per 64-deep K step instead of 16 KB + BN*128 B.
+//
+// Resident filter (p.sm.b_res, CL = 1 and one K split only): when the whole
+// [K][BN] filter block of the CTA's output-channel tile fits in shared memory
+// (K <= 256 at BN = 256: a 1x1 convolution of up to 256 input channels) it is
+// loaded once, K step by K step alongside the A tiles of the CTA's first
+// tile, and afterwards only A streams through the ring: a memory-bound
+// convolution then moves just its activations and outputs through each SM
+// instead of re-reading the filters from L2 for every tile.  The host
+// launches a multiple of num_n_tiles CTAs, so CTA c always gets channel tile
+// c % num_n_tiles.
 template <int BN, bool IM2COL, int CL, int kEpiWarps>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     conv_umma_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_y, const UmmaParams p)
 {
-    using L = Layout<BN, kEpiWarps>;
+    using T = Tile<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFFSET);
-    uint64_t *empty = full + kStages;
-    uint64_t *tfull = empty + kStages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.sm.off_bar);
+    uint64_t *empty = full + kMaxStages;
+    uint64_t *tfull = empty + kMaxStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    const int nstages = p.sm.stages;
+    const bool b_res = CL == 1 && p.sm.b_res != 0;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int crank = CL > 1 ? (int)ptx::cluster_ctarank() : 0;
     const int cid = (int)blockIdx.x / CL, ncl = (int)gridDim.x / CL;   // cluster index and count
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < nstages; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], CL);   // released by the MMA thread of every CTA of the cluster
         }
@@ -111,7 +136,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         ptx::prefetch_tensormap(&tmap_y);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(tmem_slot, L::TMEM_COLS);
+        ptx::tmem_alloc(tmem_slot, T::TMEM_COLS);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -128,6 +153,10 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             uint32_t issued = 0, last_phase = 0;  // per-stage bit masks
             bool ok = true;
             for (int work = cid; ok && work < p.num_work; work += ncl) {
+                // a resident filter block streams in with the CTA's first tile:
+                // K step kb's B tile lands in its resident slot on the same
+                // barrier as that step's A tile
+                const bool first = work == cid;
                 const int tile = work / p.splits;
                 const int kb_begin = (work - tile * p.splits) * p.kb_per_split;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
@@ -142,9 +171,10 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
-                    uint8_t *a_dst = smem + stage * L::STAGE_BYTES;
-                    uint8_t *b_dst = a_dst + L::A_BYTES;
+                    ptx::mbar_arrive_expect_tx(&full[stage],
+                                               (uint32_t)(p.sm.stage_bytes + (b_res && first ? T::B_BYTES : 0)));
+                    uint8_t *a_dst = smem + stage * p.sm.stage_bytes;
+                    uint8_t *b_dst = a_dst + kABytes;
                     const int tap = kb / p.cblocks;
                     const int c0 = (kb - tap * p.cblocks) * BK;
                     if constexpr (IM2COL) {
@@ -157,11 +187,13 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                     if constexpr (CL > 1)
                         ptx::tma_load_2d_multicast(b_dst + crank * (BN / CL) * (BK * 2), &tmap_b, &full[stage],
                                                    kb * BK, n0 + crank * (BN / CL), (uint16_t)((1u << CL) - 1));
-                    else
+                    else if (!b_res)
                         ptx::tma_load_2d(b_dst, &tmap_b, &full[stage], kb * BK, n0);
+                    else if (first)
+                        ptx::tma_load_2d(smem + p.sm.off_bres + kb * T::B_BYTES, &tmap_b, &full[stage], kb * BK, n0);
                     issued |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kStages) {
+                    if (++stage == nstages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -169,7 +201,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             }
             if (!ok) atomicOr(p.err, TF_DEVERR_PRODUCER_WAIT);
             // Every issued copy must have landed before the CTA may exit.
-            for (int s = 0; s < kStages; ++s)
+            for (int s = 0; s < nstages; ++s)
                 if ((issued >> s) & 1u)
                     if (!ptx::mbar_wait(&full[s], (last_phase >> s) & 1u, p.wait_ns))
                         atomicOr(p.err, TF_DEVERR_DRAIN_WAIT);
@@ -199,8 +231,9 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t a_addr = ptx::smem_u32(smem + stage * L::STAGE_BYTES);
-                    const uint32_t b_addr = a_addr + L::A_BYTES;
+                    const uint32_t a_addr = ptx::smem_u32(smem + stage * p.sm.stage_bytes);
+                    const uint32_t b_addr = b_res ? ptx::smem_u32(smem + p.sm.off_bres + kb * T::B_BYTES)
+                                                  : a_addr + kABytes;
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         ptx::umma_bf16(d_tmem, ptx::sw128_kmajor_desc(a_addr + k * UMMA_K * 2),
@@ -212,7 +245,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                         ptx::umma_commit_multicast(&empty[stage], (uint16_t)((1u << CL) - 1));
                     else
                         ptx::umma_commit(&empty[stage]);
-                    if (++stage == kStages) {
+                    if (++stage == nstages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -231,10 +264,17 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         // chunk becomes 32 pixels x 32 channels of bf16 in a 64-byte-swizzled
         // staging box, written to y by one TMA store.  Sixteen warps (four per
         // SM sub-partition) keep the special-function and FMA pipes busy
-        // while others wait on TMEM loads and stores.
+        // while others wait on TMEM loads and stores.  Every lane needs all 32
+        // scale and bias values of a chunk: the warp keeps those of its chunks
+        // in a shared-memory slice (one coalesced load per lane and chunk,
+        // repeated only when the tile's channel range changes) and reads them
+        // with broadcast loads.
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
-        uint8_t *box = smem + L::OUT_OFFSET + (warp - 2) * kOutBoxBytes;
+        uint8_t *box = smem + p.sm.off_out + (warp - 2) * kOutBoxBytes;
+        constexpr int kChunks = chunks_per_warp(BN, kEpiWarps);
+        float *slice = reinterpret_cast<float *>(smem + p.sm.off_par + (warp - 2) * kChunks * kParamChunkBytes);
+        int slice_n0 = -1;   // channel tile whose parameters the slice holds
         int local = 0;
         bool ok = true;
         for (int work = cid; work < p.num_work; work += ncl, ++local) {
@@ -244,6 +284,23 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             const int n0 = (tile % p.num_n_tiles) * BN;
             const int b = local & 1;
             const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
+            if (p.epilogue == 1 && n0 != slice_n0) {   // before the accumulator wait, which hides the latency
+                float sv[kChunks], bv[kChunks];
+#pragma unroll
+                for (int i = 0; i < kChunks; ++i) {
+                    const int col = n0 + (h + i * (kEpiWarps / 4)) * 32 + lane;
+                    sv[i] = __ldg(p.scale + col);
+                    bv[i] = __ldg(p.bias + col);
+                }
+                __syncwarp();   // every lane is done with the previous tile's values
+#pragma unroll
+                for (int i = 0; i < kChunks; ++i) {
+                    slice[i * 64 + lane] = sv[i];
+                    slice[i * 64 + 32 + lane] = bv[i];
+                }
+                __syncwarp();
+                slice_n0 = n0;
+            }
             const bool got = ptx::mbar_wait(&tfull[b], acc_phase, p.wait_ns);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
@@ -253,7 +310,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             const int prow = m0 + q * 32;   // first pixel of this warp's rows
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
 #pragma unroll 1
-            for (int c = h; c < BN / 32; c += kEpiWarps / 4) {
+            for (int c = h, ci = 0; c < BN / 32; c += kEpiWarps / 4, ++ci) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
                 if (p.epilogue == 2) {
@@ -269,33 +326,31 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                     }
                     continue;
                 }
+                // the store issued from this box for the previous chunk must have read it
+                if (lane == 0) ptx::bulk_wait_group_read<0>();
+                __syncwarp();
                 ptx::tmem_ld_wait();
-                uint32_t packed[16];
-                const float4 *s4 = reinterpret_cast<const float4 *>(p.scale + n0 + c * 32);
-                const float4 *b4 = reinterpret_cast<const float4 *>(p.bias + n0 + c * 32);
+                const float4 *s4 = reinterpret_cast<const float4 *>(slice + ci * 64);
+                const float4 *b4 = reinterpret_cast<const float4 *>(slice + ci * 64 + 32);
+                uint32_t wq[4];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     float2 v0 = make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]));
                     float2 v1 = make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
                     if (p.epilogue) {
-                        const float4 a4 = __ldg(s4 + j), c4 = __ldg(b4 + j);
+                        const float4 a4 = s4[j], c4 = b4[j];
                         v0 = silu_f32x2(ffma2(v0, make_float2(a4.x, a4.y), make_float2(c4.x, c4.y)));
                         v1 = silu_f32x2(ffma2(v1, make_float2(a4.z, a4.w), make_float2(c4.z, c4.w)));
                     }
                     __nv_bfloat162 t0 = __floats2bfloat162_rn(v0.x, v0.y), t1 = __floats2bfloat162_rn(v1.x, v1.y);
-                    packed[2 * j] = *reinterpret_cast<uint32_t *>(&t0);
-                    packed[2 * j + 1] = *reinterpret_cast<uint32_t *>(&t1);
-                }
-                // the store issued from this box for the previous chunk must have read it
-                if (lane == 0) ptx::bulk_wait_group_read<0>();
-                __syncwarp();
-                // row `lane`, 16-byte chunk j lands at chunk j ^ ((lane >> 1) & 3):
-                // the 64-byte swizzle the store's tensor map expects
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int pj = j ^ ((lane >> 1) & 3);
-                    *reinterpret_cast<uint4 *>(box + lane * 64 + pj * 16) =
-                        make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+                    wq[2 * (j & 1)] = *reinterpret_cast<uint32_t *>(&t0);
+                    wq[2 * (j & 1) + 1] = *reinterpret_cast<uint32_t *>(&t1);
+                    if (j & 1) {
+                        // row `lane`, 16-byte chunk j/2 lands at chunk (j/2) ^ ((lane >> 1) & 3):
+                        // the 64-byte swizzle the store's tensor map expects
+                        const int pj = (j >> 1) ^ ((lane >> 1) & 3);
+                        *reinterpret_cast<uint4 *>(box + lane * 64 + pj * 16) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                    }
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
@@ -317,7 +372,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     if constexpr (CL > 1) ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+        ptx::tmem_dealloc(tmem_base, T::TMEM_COLS);
     }
 }
 
@@ -373,19 +428,50 @@ bool is_plain_gemm(const tf_conv_shape &s)
 // positions ow*stride - pad.
 int upper_corner(int in, int out, int stride, int pad) { return (out - 1) * stride - pad - (in - 1); }
 
-template <int BN, bool IM2COL, int CL, int EPI>
-cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty, const UmmaParams &p,
-                      cudaStream_t st)
+// Shared-memory plan for BN x EPI: the resident filter block when asked for
+// and within kBResMaxBytes with at least 3 A stages left, else the plain
+// ring; as many stages as fit, up to kMaxStages.  False if fewer than two fit.
+template <int BN, int EPI>
+bool plan_smem(int num_kb, bool want_bres, SmemPlan &sm)
 {
-    using L = Layout<BN, EPI>;
+    constexpr int kFixed = EPI * (kOutBoxBytes + chunks_per_warp(BN, EPI) * kParamChunkBytes) + kBarBytes +
+                           1024;   // + alignment slack
+    constexpr int b_bytes = Tile<BN>::B_BYTES;
+    const int64_t bres_bytes = (int64_t)num_kb * b_bytes;
+    sm.b_res = want_bres && bres_bytes <= kBResMaxBytes &&
+               (kSmemLimit - kFixed - bres_bytes) / kABytes >= 3;
+    sm.stage_bytes = kABytes + (sm.b_res ? 0 : b_bytes);
+    const int64_t room = kSmemLimit - kFixed - (sm.b_res ? bres_bytes : 0);
+    sm.stages = (int)(room / sm.stage_bytes);
+    if (sm.stages > kMaxStages) sm.stages = kMaxStages;
+    if (sm.stages < 2) return false;
+    sm.off_bres = sm.stages * sm.stage_bytes;
+    sm.off_out = sm.off_bres + (sm.b_res ? (int)bres_bytes : 0);
+    sm.off_par = sm.off_out + EPI * kOutBoxBytes;
+    sm.off_bar = sm.off_par + EPI * chunks_per_warp(BN, EPI) * kParamChunkBytes;
+    sm.alloc = sm.off_bar + kBarBytes + 1024;
+    return sm.alloc <= kSmemLimit;
+}
+
+template <int BN, bool IM2COL, int CL, int EPI>
+cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty, UmmaParams p,
+                      bool want_bres, cudaStream_t st)
+{
     constexpr int kThreads = threads_for(EPI);
     auto kern = conv_umma_kernel<BN, IM2COL, CL, EPI>;
+    if (!plan_smem<BN, EPI>(p.num_kb, want_bres && CL == 1 && p.splits == 1, p.sm)) return cudaErrorNotSupported;
     // Per-function, per-device attribute; cheap enough to set on every launch.
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.sm.alloc);
     if (e != cudaSuccess) return e;
     if constexpr (CL == 1) {
-        const int grid = p.num_work < sm_count() ? p.num_work : sm_count();
-        kern<<<grid, kThreads, L::ALLOC, st>>>(ta, tb, ty, p);
+        int grid = sm_count();
+        // a resident filter block pins each CTA to one channel tile: launch a
+        // multiple of num_n_tiles CTAs so that work c, c + grid, ... keeps
+        // channel tile c % num_n_tiles
+        if (p.sm.b_res) grid = grid / p.num_n_tiles * p.num_n_tiles;
+        if (grid < 1) return cudaErrorNotSupported;
+        if (grid > p.num_work) grid = p.num_work;
+        kern<<<grid, kThreads, p.sm.alloc, st>>>(ta, tb, ty, p);
         return cudaGetLastError();
     } else {
         cudaLaunchConfig_t cfg = {};
@@ -395,7 +481,7 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = L::ALLOC;
+        cfg.dynamicSmemBytes = p.sm.alloc;
         cfg.stream = st;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -415,25 +501,43 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
 
 template <bool IM2COL, int CL, int EPI>
 cudaError_t launch_epi(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
-                       const UmmaParams &p, cudaStream_t st)
+                       const UmmaParams &p, bool want_bres, cudaStream_t st)
 {
     switch (bn) {
-    case 256: return launch_bn<256, IM2COL, CL, EPI>(ta, tb, ty, p, st);
-    case 128: return launch_bn<128, IM2COL, CL, EPI>(ta, tb, ty, p, st);
-    case 64: return launch_bn<64, IM2COL, CL, EPI>(ta, tb, ty, p, st);
-    case 32: return launch_bn<32, IM2COL, CL, EPI>(ta, tb, ty, p, st);
+    case 256: return launch_bn<256, IM2COL, CL, EPI>(ta, tb, ty, p, want_bres, st);
+    case 128: return launch_bn<128, IM2COL, CL, EPI>(ta, tb, ty, p, want_bres, st);
+    case 64: return launch_bn<64, IM2COL, CL, EPI>(ta, tb, ty, p, want_bres, st);
+    case 32: return launch_bn<32, IM2COL, CL, EPI>(ta, tb, ty, p, want_bres, st);
     default: return cudaErrorNotSupported;
     }
 }
 
+// A work item of at most 16 K blocks finishes its MMAs in about the time the
+// epilogue needs for the previous tile: such kernels get more epilogue warps.
+bool short_k(int kb_per_split) { return kb_per_split <= 16; }
+
 template <bool IM2COL, int CL>
 cudaError_t launch_im(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
-                      const UmmaParams &p, cudaStream_t st)
+                      const UmmaParams &p, bool want_bres, cudaStream_t st)
 {
-    // a work item of at most 16 K blocks finishes its MMAs in about the time
-    // the epilogue needs for the previous tile: give the epilogue more warps
-    if (p.kb_per_split <= 16) return launch_epi<IM2COL, CL, kEpiWarpsShortK>(bn, ta, tb, ty, p, st);
-    return launch_epi<IM2COL, CL, kEpiWarpsLongK>(bn, ta, tb, ty, p, st);
+    if (short_k(p.kb_per_split)) return launch_epi<IM2COL, CL, kEpiWarpsShortK>(bn, ta, tb, ty, p, want_bres, st);
+    return launch_epi<IM2COL, CL, kEpiWarpsLongK>(bn, ta, tb, ty, p, want_bres, st);
+}
+
+// Channel tile width: the widest of 256/128/64/32 dividing C_out, except that
+// a short-K kernel (sixteen epilogue warps) takes 128 instead of 256 unless
+// its whole filter block can stay resident: at 256 only three ring stages
+// would fit beside the staging boxes.
+int choose_bn(const tf_conv_shape &s, int splits, int cl)
+{
+    int bn = pick_bn(s.C_out);
+    const int num_kb = s.KH * s.KW * s.C_in / BK;
+    const int kb_per_split = (num_kb + splits - 1) / splits;
+    if (bn == 256 && short_k(kb_per_split)) {
+        const bool resident = cl == 1 && splits == 1 && (int64_t)num_kb * Tile<256>::B_BYTES <= kBResMaxBytes;
+        if (!resident) bn = 128;
+    }
+    return bn;
 }
 
 }  // namespace
@@ -460,8 +564,8 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     if (!conv_umma_supports(s, a.Ho, a.Wo)) return cudaErrorNotSupported;
     EncodeTiledFn tiled = encode_tiled();
     if (!tiled) return cudaErrorNotSupported;
-    const int bn = pick_bn(s.C_out);
     const int cl = a.cluster == 2 ? 2 : 1;
+    const int bn = choose_bn(s, a.splits > 1 ? a.splits : 1, cl);
     const int64_t M = (int64_t)s.N * a.Ho * a.Wo;
     const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
 
@@ -543,8 +647,11 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     }
     p.num_work = p.num_tiles * p.splits;
     if (p.err == nullptr) return cudaErrorInitializationError;
-    if (cl == 2) return im2col ? launch_im<true, 2>(bn, ta, tb, ty, p, st) : launch_im<false, 2>(bn, ta, tb, ty, p, st);
-    return im2col ? launch_im<true, 1>(bn, ta, tb, ty, p, st) : launch_im<false, 1>(bn, ta, tb, ty, p, st);
+    const bool want_bres = cl == 1 && p.splits == 1;
+    if (cl == 2)
+        return im2col ? launch_im<true, 2>(bn, ta, tb, ty, p, false, st) : launch_im<false, 2>(bn, ta, tb, ty, p, false, st);
+    return im2col ? launch_im<true, 1>(bn, ta, tb, ty, p, want_bres, st)
+                  : launch_im<false, 1>(bn, ta, tb, ty, p, want_bres, st);
 }
 
 // ---------------------------------------------------------------- split K

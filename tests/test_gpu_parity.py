@@ -113,6 +113,11 @@ UMMA_SHAPES = [
     synth.ConvShape(1, 12, 12, 64, 64, 3, 3, (1, 1), (0, 1)),       # padding along W only
     synth.ConvShape(4, 7, 7, 64, 64, 7, 7, (1, 1), (0, 0)),         # 1x1 output: every tap interior
     synth.ConvShape(1, 3, 3, 64, 64, 3, 3, (1, 1), (1, 1)),         # most taps in the padding
+    # filter block resident in shared memory (one K split, no pair)
+    synth.ConvShape(1, 23, 29, 256, 512, 1, 1, (1, 1), (0, 0)),     # 128 KB block, 2 channel tiles, one tile per CTA
+    synth.ConvShape(4, 56, 57, 64, 512, 1, 1, (1, 1), (0, 0)),      # 2 channel tiles, several tiles per CTA
+    synth.ConvShape(4, 41, 41, 64, 96, 3, 3, (1, 1), (1, 1)),       # 3 channel tiles of 32, several tiles per CTA
+    synth.ConvShape(1, 12, 12, 64, 256, 3, 3, (1, 1), (1, 1)),      # short K, block too big: 128-wide tiles, streamed
 ]
 
 
