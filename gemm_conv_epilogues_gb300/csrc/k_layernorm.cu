@@ -321,19 +321,27 @@ __device__ __forceinline__ float cta_sum(float v, float *red)
 // cluster owns the slice [r*slice, (r+1)*slice).  Clusters are persistent and
 // walk the rows c, c + nclusters, ...; like the CTA-per-row kernel, thread 0
 // of every CTA streams its slice of the coming rows (act and res) into a
-// shared-memory ring with bulk copies, and each thread holds 2 vectors of the
-// current row in fp32 registers, so a row is still read from HBM exactly once
-// ("a hidden width large enough to require a different row-reduction
-// strategy").  Each of the two reductions is a CTA sum followed by an
-// exchange: thread r pushes the CTA's partial into slot [rank] of CTA r with
-// st.async, which completes on CTA r's own mbarrier, and every CTA adds the
-// nranks slots in rank order (so all CTAs of the cluster get the same
-// value).  No cluster-wide barrier is taken per row.  Slots and mbarriers
-// are double-buffered by row parity: a peer can only be one row ahead, since
-// it cannot finish row i+1 without this CTA's second partial of row i+1,
-// which is sent after this CTA has read every slot of row i.
-template <bool RESIDUAL, bool AFFINE>
-__global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half *__restrict__ a,
+// shared-memory ring with bulk copies, and each thread holds NV vectors of
+// the current row in fp32 registers, so a row is still read from HBM exactly
+// once ("a hidden width large enough to require a different row-reduction
+// strategy").  Each CTA reduces its slice to
+// (sum, M2), M2 the sum of squared deviations from the slice's own mean (two
+// CTA sums), and exchanges that pair once: thread r pushes it into slot
+// [rank] of CTA r with st.async, which completes on CTA r's own mbarrier.
+// Every CTA then merges the nranks pairs in rank order with Chan et al.'s
+// pairwise update (the same statistics in every CTA, and no cancellation of
+// a one-pass sum of squares).  No cluster-wide barrier is taken per row.
+// Slots and mbarriers are double-buffered by row parity: a peer can only be
+// one row ahead, since it cannot finish row i+1 without this CTA's pair for
+// row i+1, which is sent after this CTA has read every slot of row i.
+//
+// NV = 4, REGP: 32 columns per thread with their gamma and beta in registers
+// for the whole kernel (slices of up to 8192 columns, 256 threads, two CTAs
+// per SM): the per-row cost of the reductions and the exchange is spread
+// over twice the columns of NV = 2.  NV = 2 with 1024 threads (only when
+// 16-CTA clusters cannot be had) re-reads gamma and beta for every row.
+template <bool RESIDUAL, bool AFFINE, int NV, int MAXT, bool REGP>
+__global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layernorm_cluster_kernel(const __half *__restrict__ a,
                                                                  const __half *__restrict__ b,
                                                                  const float *__restrict__ gamma,
                                                                  const float *__restrict__ beta,
@@ -341,12 +349,11 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
                                                                  int slice, float eps, int stages, uint32_t *err,
                                                                  uint64_t wait_ns)
 {
-    constexpr int NV = 2;
-    constexpr int kMaxRanks = 8;
+    constexpr int kMaxRanks = 16;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[32];
-    __shared__ float slot[2][2][kMaxRanks];   // [row parity][sum, squares][sending rank]
-    __shared__ __align__(8) uint64_t xbar[2][2];
+    __shared__ __align__(8) float2 slot[2][kMaxRanks];   // [row parity][sending rank]: (sum, M2) of its slice
+    __shared__ __align__(8) uint64_t xbar[2];
     const uint32_t rank = ptx::cluster_ctarank(), nranks = cluster_nctarank();
     const int64_t cid = blockIdx.x / nranks, ncl = gridDim.x / nranks;
     const int c0 = (int)rank * slice;                    // first column of this CTA's slice
@@ -364,8 +371,7 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
     };
     if (threadIdx.x == 0) {
         for (int st = 0; st < stages; ++st) ptx::mbar_init(&full[st], 1);
-        for (int p = 0; p < 2; ++p)
-            for (int q = 0; q < 2; ++q) ptx::mbar_init(&xbar[p][q], 1);
+        for (int p = 0; p < 2; ++p) ptx::mbar_init(&xbar[p], 1);
         ptx::mbar_init_fence();
         for (int st = 0; st < stages; ++st) {
             const int64_t row = cid + st * ncl;
@@ -375,23 +381,37 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
     }
     ptx::cluster_sync();   // every CTA's exchange barriers exist before the first push
 
-    // Sends this CTA's partial v (held by every thread) to slot[p][q][rank] of
-    // every CTA of the cluster; returns the rank-ordered sum of the nranks
-    // partials once they have all arrived here.
+    float g[NV][8], bb[NV][8];
+    auto load_params = [&](int k) {
+        const int v = threadIdx.x + k * blockDim.x;
+        const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gamma + c0 + 8 * v));
+        const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gamma + c0 + 8 * v + 4));
+        const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + c0 + 8 * v));
+        const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + c0 + 8 * v + 4));
+        g[k][0] = g0.x; g[k][1] = g0.y; g[k][2] = g0.z; g[k][3] = g0.w;
+        g[k][4] = g1.x; g[k][5] = g1.y; g[k][6] = g1.z; g[k][7] = g1.w;
+        bb[k][0] = b0.x; bb[k][1] = b0.y; bb[k][2] = b0.z; bb[k][3] = b0.w;
+        bb[k][4] = b1.x; bb[k][5] = b1.y; bb[k][6] = b1.z; bb[k][7] = b1.w;
+    };
+    if (AFFINE && REGP) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (threadIdx.x + k * blockDim.x < nvec) load_params(k);
+    }
+
+    // Sends this CTA's (sum, M2) (held by every thread) to slot[p][rank] of
+    // every CTA of the cluster and waits until all nranks pairs have arrived.
     bool xfail = false;
-    auto exchange = [&](float v, int p, int q, uint32_t parity) -> float {
-        if (threadIdx.x == 0 && !xfail) ptx::mbar_arrive_expect_tx(&xbar[p][q], nranks * 4u);
+    auto exchange = [&](float sum, float m2, int p, uint32_t parity) {
+        if (threadIdx.x == 0 && !xfail) ptx::mbar_arrive_expect_tx(&xbar[p], nranks * 8u);
         if (threadIdx.x < nranks)
-            ptx::st_async_f32(ptx::mapa_shared(&slot[p][q][rank], threadIdx.x), v,
-                              ptx::mapa_shared(&xbar[p][q], threadIdx.x));
-        const bool ok = !xfail && ptx::mbar_wait<true>(&xbar[p][q], parity, wait_ns);
+            ptx::st_async_f32x2(ptx::mapa_shared(&slot[p][rank], threadIdx.x), sum, m2,
+                                ptx::mapa_shared(&xbar[p], threadIdx.x));
+        const bool ok = !xfail && ptx::mbar_wait<true>(&xbar[p], parity, wait_ns);
         if (!ok && !xfail) {   // a peer stalled: stop using the barriers (results are void)
             xfail = true;
             atomicOr(err, TF_DEVERR_EXCHANGE_WAIT);
         }
-        float t = 0.0f;
-        for (uint32_t r = 0; r < nranks; ++r) t += slot[p][q][r];
-        return t;
     };
 
     const float inv_h = 1.0f / (float)hidden;
@@ -412,7 +432,7 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
             if (threadIdx.x == 0) atomicOr(err, TF_DEVERR_PRODUCER_WAIT);
         }
         const unsigned char *src = smem + (size_t)st * stage_bytes;
-        float s[NV][8];
+        float sv[NV][8];
         float sum = 0.0f;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -426,15 +446,15 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
             const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float2 t = __half22float2(ah[j]);
+                float2 f = __half22float2(ah[j]);
                 if (RESIDUAL) {
                     const float2 u = __half22float2(bh[j]);
-                    t.x += u.x;
-                    t.y += u.y;
+                    f.x += u.x;
+                    f.y += u.y;
                 }
-                s[k][2 * j] = t.x;
-                s[k][2 * j + 1] = t.y;
-                sum += t.x + t.y;
+                sv[k][2 * j] = f.x;
+                sv[k][2 * j + 1] = f.y;
+                sum += f.x + f.y;
             }
         }
         const float total = cta_sum(sum, red);   // its barriers also mean every thread has read stage `st`
@@ -446,39 +466,45 @@ __global__ void __launch_bounds__(1024, 1) layernorm_cluster_kernel(const __half
                 issued_until = it + stages + 1;
             }
         }
-        const float mean = exchange(total, pb, 0, xpar) * inv_h;
+        // this slice's own mean and sum of squared deviations from it ...
+        const float mean_c = total / (float)width;
         float sq = 0.0f;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             if (threadIdx.x + k * blockDim.x < nvec) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float d = s[k][j] - mean;
+                    const float d = sv[k][j] - mean_c;
                     sq = fmaf(d, d, sq);
                 }
             }
         }
-        const float rstd = rsqrtf(exchange(cta_sum(sq, red), pb, 1, xpar) * inv_h + eps);
+        exchange(total, cta_sum(sq, red), pb, xpar);
+        // ... merged over the slices (Chan et al.'s pairwise update):
+        // M2 = sum_r M2_r + sum_r n_r (mean_r - mean)^2, in rank order
+        float tsum = 0.0f;
+        for (uint32_t r = 0; r < nranks; ++r) tsum += slot[pb][r].x;
+        const float mean = tsum * inv_h;
+        float m2 = 0.0f;
+        for (uint32_t r = 0; r < nranks; ++r) {
+            const float n_r = (float)min(hidden - (int)r * slice, slice);
+            const float d = slot[pb][r].x / n_r - mean;
+            m2 += slot[pb][r].y + n_r * d * d;
+        }
+        const float rstd = rsqrtf(m2 * inv_h + eps);
         __half *yr = y + row * hidden + c0;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int v = threadIdx.x + k * blockDim.x;
             if (v >= nvec) continue;
-            float g[8], bb[8];
-            if (AFFINE) {
-                const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gamma + c0 + 8 * v));
-                const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gamma + c0 + 8 * v + 4));
-                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + c0 + 8 * v));
-                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + c0 + 8 * v + 4));
-                g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w; g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
-                bb[0] = b0.x; bb[1] = b0.y; bb[2] = b0.z; bb[3] = b0.w; bb[4] = b1.x; bb[5] = b1.y; bb[6] = b1.z; bb[7] = b1.w;
-            }
+            if (AFFINE && !REGP) load_params(k);
             uint4 out;
             __half2 *oh = reinterpret_cast<__half2 *>(&out);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float o0 = (s[k][2 * j] - mean) * rstd, o1 = (s[k][2 * j + 1] - mean) * rstd;
-                oh[j] = AFFINE ? __floats2half2_rn(fmaf(o0, g[2 * j], bb[2 * j]), fmaf(o1, g[2 * j + 1], bb[2 * j + 1]))
+                const float o0 = (sv[k][2 * j] - mean) * rstd, o1 = (sv[k][2 * j + 1] - mean) * rstd;
+                oh[j] = AFFINE ? __floats2half2_rn(fmaf(o0, g[k][2 * j], bb[k][2 * j]),
+                                                   fmaf(o1, g[k][2 * j + 1], bb[k][2 * j + 1]))
                                : __floats2half2_rn(o0, o1);
             }
             st_stream(yr + 8 * v, out);
@@ -553,28 +579,36 @@ cudaError_t launch_ln_warp(const void *a, const void *b, const float *gamma, con
     return pick(layernorm_warp_kernel<4, RESIDUAL, AFFINE>);
 }
 
-template <bool RESIDUAL, bool AFFINE>
-cudaError_t launch_ln_cluster(const void *a, const void *b, const float *gamma, const float *beta, void *y,
-                              int64_t rows, int64_t hidden, float eps, cudaStream_t st)
+// Cluster size (2..max_csize CTAs) and slice width for a row of `hidden`
+// columns cut into slices of at most about `target` columns; no CTA is left
+// with an empty slice.
+void cluster_geometry(int64_t hidden, int target, int max_csize, int &csize, int64_t &slice)
 {
-    if (hidden > kClusterMaxHidden) return cudaErrorNotSupported;
-    uint32_t *err = device_error_word();
-    if (!err) return cudaErrorInitializationError;
-    // Slices of at most 8192 values (so two CTAs fit an SM) while the cluster
-    // stays within the portable 8 CTAs; 16384 per CTA beyond 65536.
-    int csize = (int)((hidden + 8191) / 8192);
+    csize = (int)((hidden + target - 1) / target);
     if (csize < 2) csize = 2;
-    if (csize > 8) csize = 8;
-    while (csize > 1 && (csize - 1) * (((hidden + csize - 1) / csize + 7) / 8 * 8) >= hidden) --csize;  // no empty slice
-    const int64_t slice = ((hidden + csize - 1) / csize + 7) / 8 * 8;
-    const int threads = threads_for(slice, 2);
+    if (csize > max_csize) csize = max_csize;
+    while (csize > 1 && (csize - 1) * (((hidden + csize - 1) / csize + 7) / 8 * 8) >= hidden) --csize;
+    slice = ((hidden + csize - 1) / csize + 7) / 8 * 8;
+}
+
+template <bool RESIDUAL, bool AFFINE, int NV, int MAXT, bool REGP>
+cudaError_t launch_ln_cluster_with(const void *a, const void *b, const float *gamma, const float *beta, void *y,
+                                   int64_t rows, int64_t hidden, float eps, int csize, int64_t slice, uint32_t *err,
+                                   cudaStream_t st)
+{
+    const int threads = threads_for(slice, NV);
+    if (threads > MAXT) return cudaErrorNotSupported;
     const size_t stage_bytes = (size_t)slice * 2 * (RESIDUAL ? 2 : 1);
     int stages = (int)((96 * 1024) / stage_bytes);
     stages = stages < 2 ? 2 : (stages > 4 ? 4 : stages);
     const size_t smem = (size_t)stages * stage_bytes + 8 * (size_t)stages;
-    auto kern = layernorm_cluster_kernel<RESIDUAL, AFFINE>;
+    auto kern = layernorm_cluster_kernel<RESIDUAL, AFFINE, NV, MAXT, REGP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    if (e == cudaSuccess && csize > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) {
+        cudaGetLastError();   // a refused attribute is not an error of the caller's stream
+        return cudaErrorNotSupported;
+    }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -588,14 +622,37 @@ cudaError_t launch_ln_cluster(const void *a, const void *b, const float *gamma, 
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(sm_count() / csize * csize);
     int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorNotSupported;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
     if (clusters > rows) clusters = (int)rows;
     cfg.gridDim = dim3((unsigned)(clusters * csize));
     return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const __half *>(a), reinterpret_cast<const __half *>(b),
                               gamma, beta, reinterpret_cast<__half *>(y), rows, (int)hidden, (int)slice, eps, stages,
                               err, wait_limit_ns());
+}
+
+template <bool RESIDUAL, bool AFFINE>
+cudaError_t launch_ln_cluster(const void *a, const void *b, const float *gamma, const float *beta, void *y,
+                              int64_t rows, int64_t hidden, float eps, cudaStream_t st)
+{
+    if (hidden > kClusterMaxHidden) return cudaErrorNotSupported;
+    uint32_t *err = device_error_word();
+    if (!err) return cudaErrorInitializationError;
+    // Slices of at most 8192 columns (256 threads, two CTAs per SM) so that
+    // gamma and beta fit in registers: clusters of up to 8 CTAs to 65536
+    // columns, 16 beyond.  Where the GPU cannot form 16-CTA clusters,
+    // portable clusters of 8 CTAs with slices of up to 16384 columns.
+    int csize;
+    int64_t slice;
+    cluster_geometry(hidden, 8192, 16, csize, slice);
+    cudaError_t e = launch_ln_cluster_with<RESIDUAL, AFFINE, 4, 256, true>(a, b, gamma, beta, y, rows, hidden, eps,
+                                                                            csize, slice, err, st);
+    if (e != cudaErrorNotSupported) return e;
+    cluster_geometry(hidden, 8192, 8, csize, slice);
+    return launch_ln_cluster_with<RESIDUAL, AFFINE, 2, 1024, false>(a, b, gamma, beta, y, rows, hidden, eps, csize,
+                                                                    slice, err, st);
 }
 
 template <bool RESIDUAL, bool AFFINE>

@@ -142,6 +142,14 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint
                  : "memory");
 }
 
+// Two floats, 8 bytes, the same way.
+__device__ __forceinline__ void st_async_f32x2(uint32_t remote_addr, float a, float b, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(remote_addr),
+                 "f"(a), "f"(b), "r"(remote_bar)
+                 : "memory");
+}
+
 // Barrier over all threads of all CTAs of the cluster (release/acquire).
 __device__ __forceinline__ void cluster_sync()
 {
