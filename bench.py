@@ -445,6 +445,28 @@ class _Null:
         return False
 
 
+def copy_reference_gbs(nbytes: int = 1 << 30, reps: int = 20) -> float:
+    """Bytes moved per second (read + write) by a plain device-to-device copy
+    of `nbytes` through torch: context for the memory-bound kernels' GB/s,
+    not a roofline denominator."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        dst.copy_(src)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        dst.copy_(src)
+    e1.record()
+    torch.cuda.synchronize()
+    gbs = 2 * nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del src, dst
+    torch.cuda.empty_cache()
+    return gbs
+
+
 def roofline(bound, achieved, peak, unit, traffic):
     return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": traffic}
@@ -616,6 +638,10 @@ def main():
                     "SiLU kernels"}
         del pr
         torch.cuda.empty_cache()
+        workloads["hbm_copy_reference"] = {
+            "gbs": round(copy_reference_gbs(), 1),
+            "note": "torch device-to-device copy of 1 GiB (read + write bytes / time): what a plain streaming "
+                    "copy reaches on this GPU, for context beside the memory-bound kernels"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
