@@ -34,6 +34,7 @@ __device__ __forceinline__ float epilogue(float acc, int co, const float *scale,
 // warp's x reads are broadcasts and its y writes are contiguous.
 __global__ void __launch_bounds__(256) conv_direct_kernel(ConvArgs a)
 {
+    pdl_begin();
     const tf_conv_shape s = a.s;
     const int64_t total = (int64_t)s.N * a.Ho * a.Wo * s.C_out;
     const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -78,6 +79,7 @@ constexpr int TH = 8, TW = 16, CO_T = 16, CI_T = 8;
 
 __global__ void __launch_bounds__(TH * TW) conv_tiled_kernel(ConvArgs a, int halo_h, int halo_w)
 {
+    pdl_begin();
     extern __shared__ __align__(16) unsigned char smem[];
     const tf_conv_shape s = a.s;
     uint4 *xs = reinterpret_cast<uint4 *>(smem);                       // [halo_h][halo_w] x 8 channels
@@ -144,8 +146,7 @@ cudaError_t launch_conv_direct(const ConvArgs &a, cudaStream_t st)
     const int64_t total = (int64_t)a.s.N * a.Ho * a.Wo * a.s.C_out;
     const int64_t grid = (total + 255) / 256;
     if (grid > 0x7fffffff) return cudaErrorNotSupported;
-    conv_direct_kernel<<<(unsigned)grid, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(conv_direct_kernel, dim3((unsigned)grid), dim3(256), 0, st, a);
 }
 
 cudaError_t launch_conv_tiled(const ConvArgs &a, cudaStream_t st)
@@ -160,8 +161,7 @@ cudaError_t launch_conv_tiled(const ConvArgs &a, cudaStream_t st)
     }
     const dim3 grid((unsigned)(((a.Ho + TH - 1) / TH) * ((a.Wo + TW - 1) / TW)), (unsigned)s.N,
                     (unsigned)((s.C_out + CO_T - 1) / CO_T));
-    conv_tiled_kernel<<<grid, TH * TW, smem, st>>>(a, halo_h, halo_w);
-    return cudaGetLastError();
+    return launch_pdl(conv_tiled_kernel, grid, dim3(TH * TW), smem, st, a, halo_h, halo_w);
 }
 
 }  // namespace tf

@@ -143,6 +143,12 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     __syncthreads();
     ptx::tc_fence_after();
     if constexpr (CL > 1) ptx::cluster_sync();   // peers' barriers exist before any multicast
+    // The set-up above touched no global memory; from here on the kernel
+    // reads and writes it, so it waits for the stream's previous kernel
+    // (programmatic dependent launch), and lets the next one start its own
+    // set-up on SMs this grid leaves.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
@@ -463,6 +469,16 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
     // Per-function, per-device attribute; cheap enough to set on every launch.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.sm.alloc);
     if (e != cudaSuccess) return e;
+    // programmatic dependent launch: the kernel's set-up may overlap the
+    // previous kernel of the stream (it waits before touching global memory)
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = p.sm.alloc;
+    cfg.stream = st;
+    cfg.attrs = attr;
     if constexpr (CL == 1) {
         int grid = sm_count();
         // a resident filter block pins each CTA to one channel tile: launch a
@@ -471,20 +487,15 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         if (p.sm.b_res) grid = grid / p.num_n_tiles * p.num_n_tiles;
         if (grid < 1) return cudaErrorNotSupported;
         if (grid > p.num_work) grid = p.num_work;
-        kern<<<grid, kThreads, p.sm.alloc, st>>>(ta, tb, ty, p);
-        return cudaGetLastError();
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CL;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = p.sm.alloc;
-        cfg.stream = st;
-        cfg.attrs = attr;
+        cfg.gridDim = dim3((unsigned)grid);
         cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
+    } else {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = CL;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
         // persistent: as many clusters as can be resident at once (an SM left
         // without a partner in its GPC stays idle rather than starting a
         // second wave)
@@ -680,6 +691,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
                                                             const float *__restrict__ bias,
                                                             __nv_bfloat16 *__restrict__ y, int epilogue)
 {
+    pdl_begin();
     const int64_t nvec = MC / 8;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
@@ -719,9 +731,8 @@ cudaError_t launch_splitk_reduce(const float *ws, int splits, int64_t M, int C_o
         per_sm = 1;
     int64_t grid = (MC / 8 + 255) / 256;
     if (grid > (int64_t)sm_count() * per_sm) grid = (int64_t)sm_count() * per_sm;
-    splitk_reduce_kernel<<<(unsigned)grid, 256, 0, st>>>(ws, splits, MC, C_out, scale, bias,
-                                                         reinterpret_cast<__nv_bfloat16 *>(y), epilogue);
-    return cudaGetLastError();
+    return launch_pdl(splitk_reduce_kernel, dim3((unsigned)grid), dim3(256), 0, st, ws, splits, MC, C_out, scale, bias,
+                      reinterpret_cast<__nv_bfloat16 *>(y), epilogue);
 }
 
 // ---------------------------------------------------------------- wait probe

@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kThreads) bias_gelu_kernel(const uint4 *__rest
                                                              uint4 *__restrict__ y, int64_t nvec,
                                                              int64_t cvec)
 {
+    pdl_begin();
     const int64_t S = (int64_t)gridDim.x * kThreads;
     int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const bool fixed_col = S % cvec == 0;
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(kThreads) chain_kernel(const uint4 *__restrict
                                                          const float *__restrict__ p0, const float *__restrict__ p1,
                                                          uint4 *__restrict__ out, int64_t nvec, int64_t cvec)
 {
+    pdl_begin();
     const int64_t S = (int64_t)gridDim.x * kThreads;
     int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const bool fixed_col = S % cvec == 0;
@@ -242,9 +244,8 @@ cudaError_t launch_chain(const void *a, const void *b, const float *p0, const fl
     while (y) { const int64_t t = x % y; x = y; y = t; }   // gcd(cvec, threads)
     const int64_t unit = cvec / x;
     if (grid >= unit) grid = grid / unit * unit;
-    chain_kernel<OP><<<(unsigned)grid, kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(a), b, p0, p1,
-                                                           reinterpret_cast<uint4 *>(out), nvec, cvec);
-    return cudaGetLastError();
+    return launch_pdl(chain_kernel<OP>, dim3((unsigned)grid), dim3(kThreads), 0, st, reinterpret_cast<const uint4 *>(a),
+                      b, p0, p1, reinterpret_cast<uint4 *>(out), nvec, cvec);
 }
 
 // ---------------------------------------------------------------- filter pack
@@ -254,6 +255,7 @@ cudaError_t launch_chain(const void *a, const void *b, const float *p0, const fl
 __global__ void pack_filter_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
                                    int C_out, int C_in, int KH, int KW)
 {
+    pdl_begin();
     const int64_t total = (int64_t)C_out * C_in * KH * KW;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < total; o += stride) {
@@ -282,10 +284,8 @@ cudaError_t launch_bias_gelu(const void *x, const void *bias, void *y, int64_t r
     while (bq) { const int64_t t = a % bq; a = bq; bq = t; }   // gcd(cvec, threads)
     const int64_t unit = cvec / a;                             // CTAs per whole number of rows
     if (grid >= unit) grid = grid / unit * unit;
-    bias_gelu_kernel<<<(unsigned)grid, kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(x),
-                                                          reinterpret_cast<const uint4 *>(bias),
-                                                          reinterpret_cast<uint4 *>(y), nvec, cvec);
-    return cudaGetLastError();
+    return launch_pdl(bias_gelu_kernel, dim3((unsigned)grid), dim3(kThreads), 0, st, reinterpret_cast<const uint4 *>(x),
+                      reinterpret_cast<const uint4 *>(bias), reinterpret_cast<uint4 *>(y), nvec, cvec);
 }
 
 cudaError_t launch_unfused_bias_add(const void *x, const void *bias, void *t, int64_t rows,
@@ -329,9 +329,8 @@ cudaError_t launch_pack_filter(const void *w_oihw, void *w_ohwi, int C_out, int 
     int64_t g = (total + 255) / 256;
     const int64_t cap = (int64_t)sm_count() * 16;
     if (g > cap) g = cap;
-    pack_filter_kernel<<<(unsigned)g, 256, 0, st>>>(reinterpret_cast<const uint16_t *>(w_oihw),
-                                                    reinterpret_cast<uint16_t *>(w_ohwi), C_out, C_in, KH, KW);
-    return cudaGetLastError();
+    return launch_pdl(pack_filter_kernel, dim3((unsigned)g), dim3(256), 0, st, reinterpret_cast<const uint16_t *>(w_oihw),
+                      reinterpret_cast<uint16_t *>(w_ohwi), C_out, C_in, KH, KW);
 }
 
 }  // namespace tf

@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(1024) layernorm_kernel(const __half *__restric
                                                          __half *__restrict__ y, int64_t rows, int hidden,
                                                          float eps, int stages, uint32_t *err, uint64_t wait_ns)
 {
+    pdl_begin();
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[32];
     const int nvec = hidden >> 3;
@@ -215,6 +216,7 @@ __global__ void __launch_bounds__(256) layernorm_warp_kernel(const __half *__res
                                                              __half *__restrict__ y, int64_t rows, int hidden,
                                                              float eps)
 {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int nvec = hidden >> 3;
@@ -349,6 +351,7 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
                                                                  int slice, float eps, int stages, uint32_t *err,
                                                                  uint64_t wait_ns)
 {
+    pdl_begin();
     constexpr int kMaxRanks = 16;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[32];
@@ -551,10 +554,9 @@ cudaError_t launch_ln_cta(const void *a, const void *b, const float *gamma, cons
         per_sm = 1;
     int64_t grid = (int64_t)sm_count() * per_sm;
     if (grid > rows) grid = rows;
-    kern<<<(unsigned)grid, threads, smem, st>>>(reinterpret_cast<const __half *>(a), reinterpret_cast<const __half *>(b),
-                                                gamma, beta, reinterpret_cast<__half *>(y), rows, (int)hidden, eps,
-                                                stages, err, wait_limit_ns());
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(threads), smem, st, reinterpret_cast<const __half *>(a),
+                      reinterpret_cast<const __half *>(b), gamma, beta, reinterpret_cast<__half *>(y), rows,
+                      (int)hidden, eps, stages, err, wait_limit_ns());
 }
 
 template <bool RESIDUAL, bool AFFINE>
@@ -570,9 +572,9 @@ cudaError_t launch_ln_warp(const void *a, const void *b, const float *gamma, con
         int64_t grid = (int64_t)sm_count() * per_sm;
         const int64_t need = (rows + 7) / 8;
         if (grid > need) grid = need;
-        kern<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const __half *>(a), reinterpret_cast<const __half *>(b),
-                                             gamma, beta, reinterpret_cast<__half *>(y), rows, (int)hidden, eps);
-        return cudaGetLastError();
+        return launch_pdl(kern, dim3((unsigned)grid), dim3(256), 0, st, reinterpret_cast<const __half *>(a),
+                          reinterpret_cast<const __half *>(b), gamma, beta, reinterpret_cast<__half *>(y), rows,
+                          (int)hidden, eps);
     };
     if (nvec <= 32) return pick(layernorm_warp_kernel<1, RESIDUAL, AFFINE>);
     if (nvec <= 64) return pick(layernorm_warp_kernel<2, RESIDUAL, AFFINE>);
@@ -610,16 +612,18 @@ cudaError_t launch_ln_cluster_with(const void *a, const void *b, const float *ga
         return cudaErrorNotSupported;
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_begin()
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cfg.gridDim = dim3(sm_count() / csize * csize);
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {

@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kThreads, 4) rowsum_kernel(const uint4 *__rest
                                                              uint4 *__restrict__ y, float *__restrict__ rowsum,
                                                              int64_t rows, int cvec)
 {
+    pdl_begin();
     __shared__ float red[kThreads / 32][R];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t ntiles = (rows + R - 1) / R;
@@ -128,10 +129,9 @@ cudaError_t launch_rowsum(const void *x, const void *bias, void *y, float *rowsu
         const int64_t ntiles = (rows + R - 1) / R;
         int64_t grid = (int64_t)sm_count() * per_sm;
         if (grid > ntiles) grid = ntiles;
-        kern<<<(unsigned)grid, kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(x),
-                                                  reinterpret_cast<const uint4 *>(bias),
-                                                  reinterpret_cast<uint4 *>(y), rowsum, rows, (int)cvec);
-        return cudaGetLastError();
+        return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), 0, st, reinterpret_cast<const uint4 *>(x),
+                          reinterpret_cast<const uint4 *>(bias), reinterpret_cast<uint4 *>(y), rowsum, rows,
+                          (int)cvec);
     };
     const int64_t chunks = (cvec + kThreads - 1) / kThreads;
     if (chunks <= 1) return go(rowsum_kernel<FUSED, 8, 1>, 8);

@@ -150,6 +150,18 @@ __device__ __forceinline__ void st_async_f32x2(uint32_t remote_addr, float a, fl
                  : "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait: block until the grids this
+// one depends on have completed and their memory is visible (returns at once
+// when the kernel was launched without the programmatic-serialization
+// attribute).  griddep_launch_dependents: let the next kernel of the stream,
+// if it was launched with that attribute, be scheduled once every CTA of this
+// grid has said so or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Barrier over all threads of all CTAs of the cluster (release/acquire).
 __device__ __forceinline__ void cluster_sync()
 {

@@ -79,6 +79,35 @@ cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t st);
 #ifdef __CUDACC__
 namespace tf {
 
+// Programmatic dependent launch.  Every kernel of the library starts with
+// pdl_begin(): it waits until the stream's previous kernel has completed and
+// its memory is visible (at once when launched without the attribute), then
+// lets the stream's next kernel be scheduled, so that kernel's launch and
+// set-up overlap this one's tail.  Nothing before pdl_begin() may touch
+// global memory.
+__device__ __forceinline__ void pdl_begin()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// kern<<<grid, block, smem, st>>>(args...) with programmatic dependent launch allowed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;
