@@ -428,6 +428,74 @@ def test_unfused_layernorm_chain(b):
     assert np.abs(y.cpu().numpy().astype(np.float64) - ref).max() <= 1e-2
 
 
+# ---------------------------------------------------------------- stream order under programmatic launch
+#
+# Every kernel is launched with programmatic dependent launch and waits
+# (griddepcontrol.wait) before its first global-memory access.  These calls
+# run back to back on one stream without a host synchronisation between
+# them; a kernel that started touching memory too early would read a
+# half-written input (read after write) or overwrite an input the previous
+# kernel is still reading (write after read).
+
+def test_stream_order_read_after_write(b):
+    rows, cols = 4096, 8192
+    d0 = synth.bias_gelu_inputs(rows, cols, seed=30)
+    d1 = synth.bias_gelu_inputs(rows, cols, seed=31)
+    x = dev_f16(d0["x"])
+    y1 = torch.full((rows, cols), float("nan"), dtype=torch.float16, device="cuda")
+    y2 = torch.empty_like(y1)
+    y3 = torch.empty_like(y1)
+    g, be = dev_f32(np.ones(cols, np.float32)), dev_f32(d1["bias"].astype(np.float32))
+    for _ in range(3):
+        b.tf_bias_gelu(x, dev_f16(d0["bias"]), y1, rows, cols)      # y1 = GELU(x + b0)
+        b.tf_bias_gelu(y1, dev_f16(d1["bias"]), y2, rows, cols)     # reads y1 at once
+        b.tf_residual_layernorm(y2, y1, g, be, y3, rows, cols, 1e-5)   # reads both
+    torch.cuda.synchronize()
+    h1 = y1.cpu().numpy()
+    h2 = y2.cpu().numpy()
+    assert f16_ulp_distance(h2.view(np.uint16), oracle.bias_gelu(h1, d1["bias"])).max() <= 2
+    ref3 = oracle.residual_layernorm(h2, h1, np.ones(cols, np.float32), d1["bias"].astype(np.float32), eps=1e-5)
+    assert np.abs(y3.cpu().numpy().astype(np.float64) - ref3).max() <= 1e-2
+    _assert_no_device_error(b)
+
+
+def test_stream_order_write_after_read(b):
+    rows, cols = 4096, 8192
+    d0 = synth.bias_gelu_inputs(rows, cols, seed=32)
+    d1 = synth.bias_gelu_inputs(rows, cols, seed=33)
+    x = dev_f16(d0["x"])
+    z = dev_f16(d1["x"])
+    bias = dev_f16(d0["bias"])
+    y = torch.empty((rows, cols), dtype=torch.float16, device="cuda")
+    b.tf_bias_gelu(x, bias, y, rows, cols)   # reads x ...
+    b.tf_bias_gelu(z, bias, x, rows, cols)   # ... which the next call overwrites
+    torch.cuda.synchronize()
+    assert f16_ulp_distance(y.cpu().numpy().view(np.uint16), oracle.bias_gelu(d0["x"], d0["bias"])).max() <= 2
+    assert f16_ulp_distance(x.cpu().numpy().view(np.uint16), oracle.bias_gelu(d1["x"], d0["bias"])).max() <= 2
+
+
+def test_stream_order_conv_chain(b):
+    # the tensor-core conv's output feeds the next conv, whose output then
+    # overwrites the first conv's input
+    c = synth.ConvShape(2, 28, 28, 128, 128, 1, 1, (1, 1), (0, 0))
+    d = synth.conv_inputs(c, seed=34, w_dist="normal_fanin")
+    x = dev_u16(d["x"])
+    w = torch.empty((c.C_out, 1, 1, c.C_in), dtype=torch.int16, device="cuda")
+    b.tf_pack_filter_nhwc(dev_u16(d["w_oihw"]), w, c.C_out, c.C_in, 1, 1)
+    sc, bi = dev_f32(d["scale"]), dev_f32(d["bias"])
+    shape = _shape(b, c)
+    y1 = torch.empty((c.M, c.C_out), dtype=torch.int16, device="cuda")
+    b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y1, shape, b.TF_CONV_UMMA)
+    b.tf_conv2d_bn_silu_variant(y1, w, sc, bi, x, shape, b.TF_CONV_UMMA)   # reads y1, overwrites x
+    torch.cuda.synchronize()
+    h1 = host_u16(y1).reshape(c.N, c.Ho, c.Wo, c.C_out)   # bf16 words
+    ref1 = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    _conv_check(bf16_to_f64(h1), ref1)
+    ref2 = oracle.conv2d_bn_silu(h1, d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    _conv_check(bf16_to_f64(host_u16(x)).reshape(ref2.shape), ref2)
+    _assert_no_device_error(b)
+
+
 # ---------------------------------------------------------------- bounded waits
 
 def test_wait_probe_times_out_and_context_survives(b):
