@@ -132,17 +132,9 @@ __device__ __forceinline__ uint32_t mapa_shared(const void *local, uint32_t rank
     return remote;
 }
 
-// Asynchronous 4-byte store into another CTA's shared memory (addresses from
-// mapa_shared); the store completes 4 bytes of transaction on that CTA's
-// mbarrier `remote_bar`.
-__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
-                 "r"(__float_as_uint(v)), "r"(remote_bar)
-                 : "memory");
-}
-
-// Two floats, 8 bytes, the same way.
+// Asynchronous 8-byte store of two floats into another CTA's shared memory
+// (addresses from mapa_shared); the store completes 8 bytes of transaction
+// on that CTA's mbarrier `remote_bar`.
 __device__ __forceinline__ void st_async_f32x2(uint32_t remote_addr, float a, float b, uint32_t remote_bar)
 {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(remote_addr),
