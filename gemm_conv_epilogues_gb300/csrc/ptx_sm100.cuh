@@ -194,6 +194,15 @@ __device__ __forceinline__ void bulk_wait_group_read()
 // Waits until all of this thread's bulk groups have completed.
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// 1-D bulk copy shared -> global of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned), in the calling thread's current bulk group.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // 1-D bulk copy global -> shared of `bytes` (a multiple of 16, both addresses
 // 16-byte aligned); completes `bytes` on the mbarrier.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
