@@ -101,6 +101,11 @@ int check_conv_shape(const tf_conv_shape *s, int *Ho, int *Wo)
 //  - the tensor-core kernel wins wherever it can run, except on tiny
 //    reductions (K = C_in*KH*KW <= 64 and under 10 MFLOP), where its fixed
 //    cost (~3.7 us for one persistent wave) loses to the direct kernel;
+//  - for long reductions (K > 1024) over at least two waves of 128-pixel
+//    tiles it runs on CTA pairs that share each filter tile through TMA
+//    multicast: half the L2 reads of B, which measured 1.5% faster over
+//    sustained runs, where the power cap sets the clock (1837 vs 1740 MHz
+//    on the 7x7 workload), and on par in short ones;
 //  - among the CUDA-core kernels the tiled one wins from 16384 output pixels
 //    up, or with few input channels (<= 16) once there are at least ~2M
 //    output-channel-taps (M * C_out * KH * KW) to share each staged halo.
@@ -109,7 +114,8 @@ int select_variant(const tf_conv_shape &s, int Ho, int Wo)
     const int64_t M = (int64_t)s.N * Ho * Wo;
     const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
     const double flops = 2.0 * (double)M * s.C_out * (double)K;
-    if (conv_umma_supports(s, Ho, Wo) && !(K <= 64 && flops < 10.0e6)) return TF_CONV_UMMA;
+    if (conv_umma_supports(s, Ho, Wo) && !(K <= 64 && flops < 10.0e6))
+        return K > 1024 && M >= 2 * 128 * (int64_t)sm_count() ? TF_CONV_UMMA_PAIR : TF_CONV_UMMA;
     const double taps = (double)M * s.C_out * s.KH * s.KW;
     if (M >= 16384 || (s.C_in <= 16 && taps >= 2.0e6)) return TF_CONV_TILED;
     return TF_CONV_DIRECT;
@@ -145,6 +151,8 @@ bool bad_rows_cols(int64_t rows, int64_t cols) { return rows <= 0 || cols <= 0; 
 int64_t splitk_bytes(const tf_conv_shape &s, int Ho, int Wo, int *splits)
 {
     *splits = 1;
+    // only the single-CTA tensor-core kernel splits K; the dispatch picks CTA
+    // pairs only for shapes with at least two waves of tiles, which never split
     if (select_variant(s, Ho, Wo) != TF_CONV_UMMA) return 0;
     const int S = conv_umma_splits(s, Ho, Wo);
     if (S <= 1) return 0;

@@ -64,7 +64,8 @@ typedef enum {
     TF_CONV_TILED = 1,   /* output-space tiles with a shared-memory halo, CUDA cores */
     TF_CONV_UMMA = 2,    /* implicit GEMM: TMA im2col -> tcgen05.mma -> TMEM -> fused epilogue */
     TF_CONV_UMMA_PAIR = 3 /* the same on 2-CTA clusters: vertically adjacent output tiles share
-                             each filter tile, loaded half by each CTA and multicast to both */
+                             each filter tile, loaded half by each CTA and multicast to both;
+                             the dispatch's choice for long reductions over many tiles */
 } tf_conv_variant;
 
 /* Row-reduction strategies of the LayerNorm kernels (see
