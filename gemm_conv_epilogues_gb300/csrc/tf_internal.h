@@ -207,37 +207,29 @@ __device__ __forceinline__ float2 gelu_f32x2(float2 s)
     return make_float2(fmaxf(d.x, w.x), fmaxf(d.y, w.y));
 }
 // SiLU(v) = v * sigmoid(v) = v / (1 + 2^(-v*log2 e)) ("Fusing an Epilogue",
-// "The shape of it").  One ex2 per value; the reciprocal of d = 1 + 2^x runs
-// on the FMA pipe instead of the special-function unit: an integer-subtraction
-// seed (subtracting the float's bit pattern from a constant approximates
-// 1/d to within 5.1% because the bit pattern is a piecewise-linear log2),
-// then two Newton-Raphson steps r <- r + r*(1 - d*r), each squaring the
-// relative error (5.1e-2 -> 2.6e-3 -> 6.5e-6).  x is clamped to 64 so d stays
-// a normal float; for v < -44 the result is within 1e-17 of zero.
-// The seed works on -d: bits(1/d) ~ 0xFEF311C3 - bits(-d) (mod 2^32).
+// "The shape of it"): one ex2.approx and one rcp.approx per value on the
+// special-function unit (GB300's has room for both beside the epilogue's FMA
+// work).  Relative error of a few fp32 ulp; for v < -88 the exponential is
+// +inf and 1/inf gives the exact limit 0 (a signed zero), with no clamp.
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr unsigned kRcpSeed = 0xFEF311C3u;
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ float silu_f32(float v)
 {
-    const float u = ex2_approx(fminf(-kLog2e * v, 64.0f));
-    const float nd = -1.0f - u;                                   // -(1 + u)
-    float r = __uint_as_float(kRcpSeed - __float_as_uint(nd));    // ~ 1/(1 + u)
-    r = fmaf(r, fmaf(nd, r, 1.0f), r);
-    r = fmaf(r, fmaf(nd, r, 1.0f), r);
-    return v * r;
+    return v * rcp_approx(1.0f + ex2_approx(-kLog2e * v));
 }
 
 __device__ __forceinline__ float2 silu_f32x2(float2 v)
 {
     const float2 x = fmul2(v, make_float2(-kLog2e, -kLog2e));
-    const float2 u = make_float2(ex2_approx(fminf(x.x, 64.0f)), ex2_approx(fminf(x.y, 64.0f)));
-    const float2 nd = ffma2(u, make_float2(-1.0f, -1.0f), make_float2(-1.0f, -1.0f));
-    float2 r = make_float2(__uint_as_float(kRcpSeed - __float_as_uint(nd.x)),
-                           __uint_as_float(kRcpSeed - __float_as_uint(nd.y)));
-    r = ffma2(r, ffma2(nd, r, make_float2(1.0f, 1.0f)), r);
-    r = ffma2(r, ffma2(nd, r, make_float2(1.0f, 1.0f)), r);
-    return fmul2(v, r);
+    const float2 d = make_float2(1.0f + ex2_approx(x.x), 1.0f + ex2_approx(x.y));
+    return fmul2(v, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
 }
 }  // namespace tf
 #endif
