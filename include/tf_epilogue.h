@@ -74,8 +74,9 @@ typedef enum {
     TF_LN_AUTO = -1,    /* by hidden width */
     TF_LN_WARP = 0,     /* one warp per row, shuffle reductions (hidden <= 1024) */
     TF_LN_CTA = 1,      /* one CTA per row, rows streamed through a bulk-copy ring (hidden <= 16384) */
-    TF_LN_CLUSTER = 2   /* a cluster of <= 8 CTAs per row, partials exchanged through
-                           distributed shared memory (16384 < hidden <= 131072) */
+    TF_LN_CLUSTER = 2   /* a thread-block cluster per row (slices of <= 8192 columns: up to 8
+                           CTAs to 65536 columns, 16 beyond), each CTA's (sum, M2) pushed into
+                           its peers' shared memory once per row (16384 < hidden <= 131072) */
 } tf_ln_variant;
 
 /* Human-readable name of a status code (static storage). */
