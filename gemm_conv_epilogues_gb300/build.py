@@ -95,6 +95,48 @@ def _build_locked(force: bool, verbose: bool) -> str:
     return LIB
 
 
+def resource_report() -> str:
+    """Registers, spills and static shared memory of every kernel, from
+    ptxas -v of a fresh compile (nothing is linked or installed), as a
+    markdown table; kernels named by their source-level template."""
+    import re
+    import subprocess as sp
+    import tempfile
+    cc = nvcc()
+    rows = []
+    with tempfile.TemporaryDirectory() as tmp:
+        for src in _sources():
+            r = sp.run([cc] + NVCC_FLAGS + ["-Xptxas=-v", "-c", src, "-o", os.path.join(tmp, "x.o")],
+                       capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(r.stderr)
+            fn = None
+            for line in r.stderr.splitlines():
+                m = re.search(r"Compiling entry function '([^']+)'", line)
+                if m:
+                    fn = m.group(1)
+                    spill = regs = smem = None
+                    continue
+                m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+                if m and fn:
+                    spill = f"{m.group(1)}/{m.group(2)}"
+                m = re.search(r"Used (\d+) registers(?:.*?(\d+) bytes smem)?", line)
+                if m and fn:
+                    regs, smem = m.group(1), m.group(2) or "0"
+                    dm = sp.run(["c++filt", fn], capture_output=True, text=True).stdout.strip()
+                    dm = dm.replace("tf::(anonymous namespace)::", "").replace("void ", "")
+                    dm = dm[:dm.rindex(">(") + 1] if ">(" in dm else dm.split("(")[0]   # drop the parameter list
+                    rows.append((os.path.basename(src), dm, regs, spill or "0/0", smem))
+                    fn = None
+    out = ["| file | kernel | registers | spill stores/loads (bytes) | static smem (bytes) |",
+           "|---|---|---:|---:|---:|"]
+    out += [f"| {f} | `{k}` | {r} | {sp_} | {sm} |" for f, k, r, sp_, sm in rows]
+    return "\n".join(out)
+
+
 if __name__ == "__main__":
     import sys
-    print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--resources" in sys.argv:
+        print(resource_report())
+    else:
+        print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv))

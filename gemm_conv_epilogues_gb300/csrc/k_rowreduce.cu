@@ -43,8 +43,11 @@ __device__ __forceinline__ void st_stream(void *p, uint4 v)
 // of them (C = ceil(cvec / 256)), so R * C = 8 independent 16-byte loads are in
 // flight per thread, and small R keeps the tiles fine-grained enough to spread
 // evenly over the persistent CTAs.
+// (The fused kernels on tiles of 4 or 8 rows keep that many row sums and
+// their GELU temporaries beside the 32 loaded values; they get the registers
+// of three CTAs per SM.)
 template <bool FUSED, int R, int C>
-__global__ void __launch_bounds__(kThreads, 4) rowsum_kernel(const uint4 *__restrict__ x,
+__global__ void __launch_bounds__(kThreads, FUSED && R >= 4 ? 3 : 4) rowsum_kernel(const uint4 *__restrict__ x,
                                                              const uint4 *__restrict__ bias,
                                                              uint4 *__restrict__ y, float *__restrict__ rowsum,
                                                              int64_t rows, int cvec)
