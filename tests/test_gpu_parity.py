@@ -227,7 +227,10 @@ def test_producer_consumer_pair(b, standalone):
 
 # ---------------------------------------------------------------- bias + GELU
 
-@pytest.mark.parametrize("rows,cols", [(1, 8), (3, 24), (37, 200), (129, 1032), (8192, 8192)])
+# rows of up to 16384 columns take the bulk-copy ring (chunks of whole rows,
+# ragged last chunks at 37x200 and 129x1032); wider rows the grid-stride kernel
+@pytest.mark.parametrize("rows,cols", [(1, 8), (3, 24), (37, 200), (129, 1032), (8192, 8192), (5, 16384),
+                                       (3, 16392), (2, 40000)])
 def test_bias_gelu(b, rows, cols):
     d = synth.bias_gelu_inputs(rows, cols, seed=5)
     y = torch.empty((rows, cols), dtype=torch.float16, device="cuda")
@@ -291,9 +294,9 @@ def test_bias_gelu_rowsum_split(b, rows, cols):
 
 
 def test_bias_gelu_beyond_2_to_31_elements(b):
-    # 262144 x 8200 = 2.15e9 values (64-bit indexing; 8200 / 8 = 1025 vectors
-    # per row, so the grid stride is not a multiple of the row and each vector
-    # reloads its bias).  The rows repeat a seeded 4096-row block on the device.
+    # 262144 x 8200 = 2.15e9 values: 64-bit offsets, one 16400-byte row per
+    # chunk of the bulk-copy ring.  The rows repeat a seeded 4096-row block on
+    # the device.
     rows, cols, block = 262144, 8200, 4096
     d = synth.bias_gelu_inputs(block, cols, seed=16)
     x = dev_f16(d["x"]).repeat(rows // block, 1)
