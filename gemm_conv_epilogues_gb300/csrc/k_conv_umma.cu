@@ -9,16 +9,19 @@
 // the padding), which is the TMA_LOAD_IM2COL -> UMMA path that page describes;
 // a 1x1 stride-1 unpadded convolution is a plain matrix, loaded as a 2-D tile.
 //
-// Persistent kernel, one CTA per SM, eighteen warps:
-//   warp 0  TMA producer: a ring of 4 shared-memory stages (A 16 KB + B BN*128 B)
+// Persistent kernel, one CTA (or, with CL = 2, one CTA pair) per SM, with
+// 2 + EPI warps:
+//   warp 0  TMA producer: a ring of up to 6 shared-memory stages sized by the
+//           host's shared-memory plan (A 16 KB + B BN*128 B per stage, or A
+//           alone when the filter block is resident)
 //   warp 1  TMEM allocator and MMA issuer: tcgen05.mma M=128, N=BN, K=16, fp32
 //           accumulators in TMEM, double-buffered so the epilogue of one tile
 //           overlaps the main loop of the next
-//   warps 2-17 epilogue ("Fusing an Epilogue", "The shape of it"): TMEM ->
-//           registers, v = acc*scale[co] + bias[co], v*sigmoid(v), bf16, then
-//           a swizzled shared-memory box and a TMA store.
-//           The per-channel parameters are read inside the kernel, as in the
-//           page's BatchNorm-epilog listing.
+//   warps 2.. epilogue ("Fusing an Epilogue", "The shape of it"), 16 warps for
+//           short K loops and 8 for long ones: TMEM -> registers,
+//           v = acc*scale[co] + bias[co], v*sigmoid(v), bf16, then a swizzled
+//           shared-memory box and a TMA store.  The per-channel parameters are
+//           read inside the kernel, as in the page's BatchNorm-epilog listing.
 // Every mbarrier wait is bounded (see ptx::mbar_wait); a role that times out
 // sets the device error word and winds down, and the CTA drains its in-flight
 // copies and MMAs before it frees TMEM and exits.
