@@ -1,0 +1,102 @@
+"""GPU parity on seeded random shapes: every conv kernel the shape admits
+(and the dispatch's own choice), bias + GELU at random widths on both sides of
+the bulk-copy ring's 16384-column limit, and residual LayerNorm at random
+widths under every row-reduction strategy that takes the width.  Same
+oracle, same tolerances as test_gpu_parity.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_conv_epilogues_gb300 import synth
+from helpers import bf16_to_f64, dev_f16, dev_f32, dev_u16, f16_ulp_distance, host_u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def b(cuda_ready):
+    from gemm_conv_epilogues_gb300 import binding
+    return binding
+
+
+def _random_convs(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        kh, kw = (int(v) for v in rng.choice([1, 3, 5, 7], 2))
+        sh, sw = (int(v) for v in rng.choice([1, 2], 2))
+        ph, pw = int(rng.integers(0, kh // 2 + 1)), int(rng.integers(0, kw // 2 + 1))
+        N = int(rng.integers(1, 3))
+        H, W = int(rng.integers(3, 21)), int(rng.integers(3, 21))
+        c_in = int(rng.choice([8, 16, 24, 64, 128]))
+        c_out = int(rng.choice([8, 16, 32, 48, 64, 96, 128, 256]))
+        c = synth.ConvShape(N, H, W, c_in, c_out, kh, kw, (sh, sw), (ph, pw))
+        if c.Ho >= 1 and c.Wo >= 1:
+            out.append(c)
+    return out
+
+
+CONVS = _random_convs(24, seed=2024)
+
+
+@pytest.mark.parametrize("c", CONVS, ids=lambda c: f"{c.N}x{c.H}x{c.W}x{c.C_in}-{c.C_out}k{c.KH}{c.KW}"
+                                                   f"s{c.stride[0]}{c.stride[1]}p{c.pad[0]}{c.pad[1]}")
+def test_conv_random_shape_every_kernel(b, c):
+    d = synth.conv_inputs(c, seed=40, w_dist="normal_fanin")
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    x = dev_u16(d["x"])
+    w = torch.empty((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device="cuda")
+    b.tf_pack_filter_nhwc(dev_u16(d["w_oihw"]), w, c.C_out, c.C_in, c.KH, c.KW)
+    sc, bi = dev_f32(d["scale"]), dev_f32(d["bias"])
+    shape = b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad)
+    variants = [b.TF_CONV_AUTO, b.TF_CONV_DIRECT, b.TF_CONV_TILED]
+    if c.C_in % 64 == 0 and c.C_out % 32 == 0:
+        variants += [b.TF_CONV_UMMA, b.TF_CONV_UMMA_PAIR]
+    for v in variants:
+        y = torch.full((c.M, c.C_out), 0x7FC0, dtype=torch.int16, device="cuda")   # NaN sentinel
+        b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v)
+        torch.cuda.synchronize()
+        got = bf16_to_f64(host_u16(y)).reshape(ref.shape)
+        err = np.abs(got - ref)
+        bad = err > 1e-2 + 1e-2 * np.abs(ref)
+        assert not bad.any(), f"variant {v}: {bad.sum()} outside tolerance, worst {err.max():.4g}"
+    rc, word = b.tf_read_device_error()
+    assert rc == b.TF_OK and word == 0
+
+
+def _random_widths(n, seed, hi):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(1, 64)), 8 * int(rng.integers(1, hi // 8 + 1))) for _ in range(n)]
+
+
+@pytest.mark.parametrize("rows,cols", _random_widths(12, seed=7, hi=24000))
+def test_bias_gelu_random_width(b, rows, cols):
+    d = synth.bias_gelu_inputs(rows, cols, seed=41)
+    y = torch.empty((rows, cols), dtype=torch.float16, device="cuda")
+    b.tf_bias_gelu(dev_f16(d["x"]), dev_f16(d["bias"]), y, rows, cols)
+    torch.cuda.synchronize()
+    ulp = f16_ulp_distance(y.cpu().numpy().view(np.uint16), oracle.bias_gelu(d["x"], d["bias"]))
+    assert ulp.max() <= 2
+
+
+@pytest.mark.parametrize("rows,hidden", _random_widths(12, seed=8, hi=48000))
+def test_layernorm_random_width_every_strategy(b, rows, hidden):
+    d = synth.layernorm_inputs(rows, hidden, seed=42)
+    ref = oracle.residual_layernorm(d["act"], d["res"], d["gamma"], d["beta"], eps=1e-5)
+    act, res = dev_f16(d["act"]), dev_f16(d["res"])
+    g, be = dev_f32(d["gamma"]), dev_f32(d["beta"])
+    ran = 0
+    for v in (b.TF_LN_AUTO, b.TF_LN_WARP, b.TF_LN_CTA, b.TF_LN_CLUSTER):
+        y = torch.full((rows, hidden), float("nan"), dtype=torch.float16, device="cuda")
+        rc = b.tf_residual_layernorm_variant(act, res, g, be, y, rows, hidden, 1e-5, v, check=False)
+        if rc == b.TF_ERR_UNSUPPORTED:   # the strategy does not take this width
+            continue
+        assert rc == b.TF_OK, (v, rc)
+        torch.cuda.synchronize()
+        err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+        assert err.max() <= 1e-2, (v, err.max())
+        ran += 1
+    assert ran >= 2   # the dispatch's choice and at least that strategy forced
+    rc, word = b.tf_read_device_error()
+    assert rc == b.TF_OK and word == 0
