@@ -100,3 +100,53 @@ def test_layernorm_random_width_every_strategy(b, rows, hidden):
     assert ran >= 2   # the dispatch's choice and at least that strategy forced
     rc, word = b.tf_read_device_error()
     assert rc == b.TF_OK and word == 0
+
+
+def test_calls_captured_in_a_cuda_graph(b):
+    # conv -> bias+GELU -> LayerNorm captured once (programmatic launches become
+    # graph edges) and replayed three times on new inputs; each replay matches
+    # the oracle
+    c = synth.ConvShape(2, 16, 16, 64, 128, 3, 3, (1, 1), (1, 1))
+    w = torch.empty((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device="cuda")
+    d0 = synth.conv_inputs(c, seed=50, w_dist="normal_fanin")
+    b.tf_pack_filter_nhwc(dev_u16(d0["w_oihw"]), w, c.C_out, c.C_in, c.KH, c.KW)
+    sc, bi = dev_f32(d0["scale"]), dev_f32(d0["bias"])
+    shape = b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad)
+    rows, cols = 64, 4096
+    x = torch.empty((c.N, c.H, c.W, c.C_in), dtype=torch.int16, device="cuda")
+    y = torch.empty((c.M, c.C_out), dtype=torch.int16, device="cuda")
+    g_in = torch.empty((rows, cols), dtype=torch.float16, device="cuda")
+    g_bias = torch.empty((cols,), dtype=torch.float16, device="cuda")
+    g_out = torch.empty_like(g_in)
+    res = torch.empty_like(g_in)
+    gam = torch.empty((cols,), dtype=torch.float32, device="cuda")
+    bet = torch.empty_like(gam)
+    ln_out = torch.empty_like(g_in)
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        s = torch.cuda.current_stream()
+        b.tf_conv2d_bn_silu(x, w, sc, bi, y, shape, stream=s)
+        b.tf_bias_gelu(g_in, g_bias, g_out, rows, cols, stream=s)
+        b.tf_residual_layernorm(g_out, res, gam, bet, ln_out, rows, cols, 1e-5, stream=s)
+    for k in range(3):
+        d = synth.conv_inputs(c, seed=51 + k, w_dist="normal_fanin")
+        e = synth.bias_gelu_inputs(rows, cols, seed=61 + k)
+        f = synth.layernorm_inputs(rows, cols, seed=71 + k)
+        x.copy_(dev_u16(d["x"]))
+        g_in.copy_(dev_f16(e["x"]))
+        g_bias.copy_(dev_f16(e["bias"]))
+        res.copy_(dev_f16(f["res"]))
+        gam.copy_(dev_f32(f["gamma"]))
+        bet.copy_(dev_f32(f["beta"]))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = oracle.conv2d_bn_silu(d["x"], d0["w_oihw"], d0["scale"], d0["bias"], c.stride, c.pad)
+        got = bf16_to_f64(host_u16(y)).reshape(ref.shape)
+        assert np.all(np.abs(got - ref) <= 1e-2 + 1e-2 * np.abs(ref))
+        assert f16_ulp_distance(g_out.cpu().numpy().view(np.uint16), oracle.bias_gelu(e["x"], e["bias"])).max() <= 2
+        ref_ln = oracle.residual_layernorm(g_out.cpu().numpy(), f["res"], f["gamma"], f["beta"], eps=1e-5)
+        assert np.abs(ln_out.cpu().numpy().astype(np.float64) - ref_ln).max() <= 1e-2
+    rc, word = b.tf_read_device_error()
+    assert rc == b.TF_OK and word == 0
