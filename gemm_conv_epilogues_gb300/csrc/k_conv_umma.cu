@@ -82,6 +82,11 @@ struct UmmaParams {
     int num_kb, cblocks, num_n_tiles, num_tiles;
     int epilogue;            // 0: plain bf16 store, 1: BN + SiLU, 2: fp32 split-K partial to ws
     int splits, kb_per_split, num_work;   // work item = (tile, K split), split fastest
+    // Items from split_from on are half tiles (BN/2 channels): item
+    // split_from + 2*i + h is half h of tile split_from + i.  Only with a
+    // resident filter block, one channel tile and one K split, so that the
+    // last, partial wave of tiles is spread over twice as many CTAs.
+    int split_from;
     float *ws;               // split-K partials [splits][M][C_out] (epilogue 2 only)
     SmemPlan sm;
 };
@@ -166,8 +171,9 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 // K step kb's B tile lands in its resident slot on the same
                 // barrier as that step's A tile
                 const bool first = work == cid;
-                const int tile = work / p.splits;
-                const int kb_begin = (work - tile * p.splits) * p.kb_per_split;
+                const int tile = work < p.split_from ? work / p.splits
+                                                     : p.split_from + (work - p.split_from) / 2;
+                const int kb_begin = work < p.split_from ? (work - tile * p.splits) * p.kb_per_split : 0;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
                 const int m0 = ((tile / p.num_n_tiles) * CL + crank) * BM;
                 const int n0 = (tile % p.num_n_tiles) * BN;
@@ -219,13 +225,18 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+            constexpr uint32_t idesc_half = ptx::idesc_bf16_f32(BM, BN / 2);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
             for (int work = cid; ok && work < p.num_work; work += ncl, ++local) {
-                const int kb_begin = (work % p.splits) * p.kb_per_split;
+                const int kb_begin = work < p.split_from ? (work % p.splits) * p.kb_per_split : 0;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
+                // a half tile: N = BN/2 on rows [half*BN/2, +BN/2) of the resident block
+                const int half = work < p.split_from ? -1 : (work - p.split_from) & 1;
+                const uint32_t id = half < 0 ? idesc : idesc_half;
+                const uint32_t b_half = half > 0 ? (uint32_t)(BN / 2) * (BK * 2) : 0u;
                 const int b = local & 1;
                 const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
                 if (!ptx::mbar_wait(&tempty[b], acc_phase ^ 1u, p.wait_ns)) {
@@ -241,12 +252,12 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t a_addr = ptx::smem_u32(smem + stage * p.sm.stage_bytes);
-                    const uint32_t b_addr = b_res ? ptx::smem_u32(smem + p.sm.off_bres + kb * T::B_BYTES)
+                    const uint32_t b_addr = b_res ? ptx::smem_u32(smem + p.sm.off_bres + kb * T::B_BYTES) + b_half
                                                   : a_addr + kABytes;
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         ptx::umma_bf16(d_tmem, ptx::sw128_kmajor_desc(a_addr + k * UMMA_K * 2),
-                                       ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2), idesc,
+                                       ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2), id,
                                        (kb > kb_begin || k > 0) ? 1u : 0u);
                     }
                     // frees the stage (in every CTA of the cluster) once these MMAs have read it
@@ -283,23 +294,27 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         uint8_t *box = smem + p.sm.off_out + (warp - 2) * kOutBoxBytes;
         constexpr int kChunks = chunks_per_warp(BN, kEpiWarps);
         float *slice = reinterpret_cast<float *>(smem + p.sm.off_par + (warp - 2) * kChunks * kParamChunkBytes);
-        int slice_n0 = -1;   // channel tile whose parameters the slice holds
+        int slice_n0 = -1;   // 2 * first channel + (half tile) of the parameters the slice holds
         int local = 0;
         bool ok = true;
         for (int work = cid; work < p.num_work; work += ncl, ++local) {
-            const int tile = work / p.splits;
-            const int split = work - tile * p.splits;
+            const int half = work < p.split_from ? -1 : (work - p.split_from) & 1;
+            const int tile = half < 0 ? work / p.splits : p.split_from + (work - p.split_from) / 2;
+            const int split = half < 0 ? work - tile * p.splits : 0;
             const int m0 = ((tile / p.num_n_tiles) * CL + crank) * BM;
-            const int n0 = (tile % p.num_n_tiles) * BN;
+            const int n0 = (tile % p.num_n_tiles) * BN + (half > 0 ? BN / 2 : 0);
+            const int width = half < 0 ? BN : BN / 2;   // channels of this item
             const int b = local & 1;
             const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-            if (p.epilogue == 1 && n0 != slice_n0) {   // before the accumulator wait, which hides the latency
+            const int slice_key = 2 * n0 + (half >= 0);   // the channels and width the slice must hold
+            if (p.epilogue == 1 && slice_key != slice_n0) {   // before the accumulator wait, which hides the latency
                 float sv[kChunks], bv[kChunks];
 #pragma unroll
                 for (int i = 0; i < kChunks; ++i) {
-                    const int col = n0 + (h + i * (kEpiWarps / 4)) * 32 + lane;
-                    sv[i] = __ldg(p.scale + col);
-                    bv[i] = __ldg(p.bias + col);
+                    const int c = h + i * (kEpiWarps / 4);
+                    // chunks past the item's width (a half tile's) are left as they are
+                    sv[i] = c * 32 < width ? __ldg(p.scale + n0 + c * 32 + lane) : 0.0f;
+                    bv[i] = c * 32 < width ? __ldg(p.bias + n0 + c * 32 + lane) : 0.0f;
                 }
                 __syncwarp();   // every lane is done with the previous tile's values
 #pragma unroll
@@ -308,7 +323,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                     slice[i * 64 + 32 + lane] = bv[i];
                 }
                 __syncwarp();
-                slice_n0 = n0;
+                slice_n0 = slice_key;
             }
             const bool got = ptx::mbar_wait(&tfull[b], acc_phase, p.wait_ns);
             if (!__all_sync(0xffffffffu, got)) {
@@ -319,7 +334,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             const int prow = m0 + q * 32;   // first pixel of this warp's rows
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
 #pragma unroll 1
-            for (int c = h, ci = 0; c < BN / 32; c += kEpiWarps / 4, ++ci) {
+            for (int c = h, ci = 0; c * 32 < width; c += kEpiWarps / 4, ++ci) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
                 if (p.epilogue == 2) {
@@ -489,6 +504,15 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         // channel tile c % num_n_tiles
         if (p.sm.b_res) grid = grid / p.num_n_tiles * p.num_n_tiles;
         if (grid < 1) return cudaErrorNotSupported;
+        // the last, partial wave of tiles as half tiles over twice the CTAs,
+        // when it then still fits in one wave (resident block, one channel tile)
+        if (p.sm.b_res && p.num_n_tiles == 1 && p.splits == 1 && BN >= 64) {
+            const int rem = p.num_tiles % grid;
+            if (rem > 0 && 2 * rem <= grid) {
+                p.split_from = p.num_tiles - rem;
+                p.num_work = p.split_from + 2 * rem;
+            }
+        }
         if (grid > p.num_work) grid = p.num_work;
         cfg.gridDim = dim3((unsigned)grid);
         cfg.numAttrs = 1;
@@ -660,6 +684,7 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
         p.ws = a.ws;
     }
     p.num_work = p.num_tiles * p.splits;
+    p.split_from = p.num_work;   // no half tiles unless launch_bn decides so
     if (p.err == nullptr) return cudaErrorInitializationError;
     const bool want_bres = cl == 1 && p.splits == 1;
     if (cl == 2)
