@@ -82,11 +82,11 @@ struct UmmaParams {
     int num_kb, cblocks, num_n_tiles, num_tiles;
     int epilogue;            // 0: plain bf16 store, 1: BN + SiLU, 2: fp32 split-K partial to ws
     int splits, kb_per_split, num_work;   // work item = (tile, K split), split fastest
-    // Items from split_from on are half tiles (BN/2 channels): item
-    // split_from + 2*i + h is half h of tile split_from + i.  Only with a
-    // resident filter block, one channel tile and one K split, so that the
-    // last, partial wave of tiles is spread over twice as many CTAs.
-    int split_from;
+    // Items from split_from on are parts of tiles (BN/parts channels each):
+    // item split_from + parts*i + j is part j of tile split_from + i.  Only
+    // with a resident filter block, one channel tile and one K split, so that
+    // the last, partial wave of tiles is spread over `parts` times the CTAs.
+    int split_from, parts;
     float *ws;               // split-K partials [splits][M][C_out] (epilogue 2 only)
     SmemPlan sm;
 };
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 // barrier as that step's A tile
                 const bool first = work == cid;
                 const int tile = work < p.split_from ? work / p.splits
-                                                     : p.split_from + (work - p.split_from) / 2;
+                                                     : p.split_from + (work - p.split_from) / p.parts;
                 const int kb_begin = work < p.split_from ? (work - tile * p.splits) * p.kb_per_split : 0;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
                 const int m0 = ((tile / p.num_n_tiles) * CL + crank) * BM;
@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
             constexpr uint32_t idesc_half = ptx::idesc_bf16_f32(BM, BN / 2);
+            constexpr uint32_t idesc_quarter = ptx::idesc_bf16_f32(BM, BN / 4);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -233,10 +234,10 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             for (int work = cid; ok && work < p.num_work; work += ncl, ++local) {
                 const int kb_begin = work < p.split_from ? (work % p.splits) * p.kb_per_split : 0;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
-                // a half tile: N = BN/2 on rows [half*BN/2, +BN/2) of the resident block
-                const int half = work < p.split_from ? -1 : (work - p.split_from) & 1;
-                const uint32_t id = half < 0 ? idesc : idesc_half;
-                const uint32_t b_half = half > 0 ? (uint32_t)(BN / 2) * (BK * 2) : 0u;
+                // part j of a tile: N = BN/parts on rows [j*BN/parts, +BN/parts) of the resident block
+                const int part = work < p.split_from ? -1 : (work - p.split_from) % p.parts;
+                const uint32_t id = part < 0 ? idesc : (p.parts == 2 ? idesc_half : idesc_quarter);
+                const uint32_t b_half = part > 0 ? (uint32_t)(part * (BN / p.parts)) * (BK * 2) : 0u;
                 const int b = local & 1;
                 const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
                 if (!ptx::mbar_wait(&tempty[b], acc_phase ^ 1u, p.wait_ns)) {
@@ -294,25 +295,25 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         uint8_t *box = smem + p.sm.off_out + (warp - 2) * kOutBoxBytes;
         constexpr int kChunks = chunks_per_warp(BN, kEpiWarps);
         float *slice = reinterpret_cast<float *>(smem + p.sm.off_par + (warp - 2) * kChunks * kParamChunkBytes);
-        int slice_n0 = -1;   // 2 * first channel + (half tile) of the parameters the slice holds
+        int slice_n0 = -1;   // 8 * first channel + parts of the item whose parameters the slice holds
         int local = 0;
         bool ok = true;
         for (int work = cid; work < p.num_work; work += ncl, ++local) {
-            const int half = work < p.split_from ? -1 : (work - p.split_from) & 1;
-            const int tile = half < 0 ? work / p.splits : p.split_from + (work - p.split_from) / 2;
-            const int split = half < 0 ? work - tile * p.splits : 0;
+            const int part = work < p.split_from ? -1 : (work - p.split_from) % p.parts;
+            const int tile = part < 0 ? work / p.splits : p.split_from + (work - p.split_from) / p.parts;
+            const int split = part < 0 ? work - tile * p.splits : 0;
+            const int width = part < 0 ? BN : BN / p.parts;   // channels of this item
             const int m0 = ((tile / p.num_n_tiles) * CL + crank) * BM;
-            const int n0 = (tile % p.num_n_tiles) * BN + (half > 0 ? BN / 2 : 0);
-            const int width = half < 0 ? BN : BN / 2;   // channels of this item
+            const int n0 = (tile % p.num_n_tiles) * BN + (part > 0 ? part * width : 0);
             const int b = local & 1;
             const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-            const int slice_key = 2 * n0 + (half >= 0);   // the channels and width the slice must hold
+            const int slice_key = 8 * n0 + (part < 0 ? 0 : p.parts);   // the channels and width the slice must hold
             if (p.epilogue == 1 && slice_key != slice_n0) {   // before the accumulator wait, which hides the latency
                 float sv[kChunks], bv[kChunks];
 #pragma unroll
                 for (int i = 0; i < kChunks; ++i) {
                     const int c = h + i * (kEpiWarps / 4);
-                    // chunks past the item's width (a half tile's) are left as they are
+                    // chunks past the item's width (a tile part's) are not needed
                     sv[i] = c * 32 < width ? __ldg(p.scale + n0 + c * 32 + lane) : 0.0f;
                     bv[i] = c * 32 < width ? __ldg(p.bias + n0 + c * 32 + lane) : 0.0f;
                 }
@@ -504,13 +505,18 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         // channel tile c % num_n_tiles
         if (p.sm.b_res) grid = grid / p.num_n_tiles * p.num_n_tiles;
         if (grid < 1) return cudaErrorNotSupported;
-        // the last, partial wave of tiles as half tiles over twice the CTAs,
-        // when it then still fits in one wave (resident block, one channel tile)
+        // the last, partial wave of tiles as quarter or half tiles over 4 or 2
+        // times the CTAs, when that still fits in one wave (resident block,
+        // one channel tile; measured 2-2.5% off the 1x1 workload's time)
         if (p.sm.b_res && p.num_n_tiles == 1 && p.splits == 1 && BN >= 64) {
             const int rem = p.num_tiles % grid;
-            if (rem > 0 && 2 * rem <= grid) {
-                p.split_from = p.num_tiles - rem;
-                p.num_work = p.split_from + 2 * rem;
+            for (int parts : {4, 2}) {
+                if (rem > 0 && parts * rem <= grid && BN / parts >= 32) {
+                    p.split_from = p.num_tiles - rem;
+                    p.parts = parts;
+                    p.num_work = p.split_from + parts * rem;
+                    break;
+                }
             }
         }
         if (grid > p.num_work) grid = p.num_work;
@@ -684,7 +690,8 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
         p.ws = a.ws;
     }
     p.num_work = p.num_tiles * p.splits;
-    p.split_from = p.num_work;   // no half tiles unless launch_bn decides so
+    p.split_from = p.num_work;   // no tile parts unless launch_bn decides so
+    p.parts = 1;
     if (p.err == nullptr) return cudaErrorInitializationError;
     const bool want_bres = cl == 1 && p.splits == 1;
     if (cl == 2)
