@@ -474,6 +474,31 @@ def roofline(bound, achieved, peak, unit, traffic):
 
 # ---------------------------------------------------------------- CPU baseline (the oracle)
 
+def cpu_oracle_full(r: "Runner") -> dict:
+    """The fp64 oracle, as it stands, on the whole of a (small or memory-bound)
+    workload's seeded inputs, on every host core: the baseline the GPU kernel
+    sits beside, in the same units."""
+    import oracle
+    d, w = r.inputs, r.w
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    if w.kind == "conv":
+        c = w.conv
+        oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad, nthreads=threads)
+    elif w.kind == "bias_gelu":
+        oracle.bias_gelu(d["x"], d["bias"], nthreads=threads)
+    elif w.kind == "bias_gelu_rowsum":
+        oracle.bias_gelu_rowsum(d["x"], d["bias"], nthreads=threads)
+    else:
+        oracle.residual_layernorm(d["act"], d["res"], d["gamma"], d["beta"], eps=1e-5, nthreads=threads)
+    dt = time.perf_counter() - t0
+    out = {"kind": "oracle", "cores": threads, "sample": "the whole workload", "seconds": round(dt, 3),
+           "gbs": round(r.alg_bytes / dt / 1e9, 3)}
+    if r.flops:
+        out["tflops"] = r.flops / dt / 1e12
+    return out
+
+
 _HEADLINE_INPUTS = {}
 
 
@@ -622,6 +647,8 @@ def main():
                      "l2": f"{r.nsets} rotating buffer sets"}
             if r.flops:
                 entry["fused"]["tflops"] = r.flops / (f_ms * 1e-3) / 1e12
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                entry["cpu_oracle"] = cpu_oracle_full(r)
             if name.startswith("conv3x3_tiny"):
                 entry["note"] = "launch-latency bound (0.59 MFLOP); reported as latency"
                 entry["fused"]["graph_us_per_call"] = graph_time_us(r.fused, 200)
