@@ -417,6 +417,19 @@ def time_loop(fn, steps: int, warmup: int, world: int, clocks=None):
     return max_over_ranks(ms, world), launches
 
 
+def time_alternating(fa, fb, steps: int, warmup: int, world: int, blocks: int = 3):
+    """Times fa and fb in alternating blocks of `steps` calls (a, b, a, b, ...),
+    each block by time_loop, and returns the median ms per call of each.  On a
+    power-capped GPU the clock depends on how long the load has lasted, so the
+    two sides of a comparison are measured over the same windows."""
+    import statistics
+    ta, tb = [], []
+    for k in range(blocks):
+        ta.append(time_loop(fa, steps, warmup, world)[0])
+        tb.append(time_loop(fb, steps, warmup, world)[0])
+    return statistics.median(ta), statistics.median(tb)
+
+
 def graph_time_us(fn, calls: int) -> float:
     """GPU time per call with `calls` calls captured in one CUDA graph and
     replayed, so the host's per-call launch cost is not counted."""
@@ -623,10 +636,13 @@ def main():
         raise SystemExit(f"device error word {word:#x} after the timed region")
 
     workloads = {}
-    unf_ms, _ = time_loop(head.unfused, max(20, args.steps // 10), args.warmup, world)
+    cmp_steps = max(20, args.steps // 10)
+    f_cmp_ms, unf_ms = time_alternating(head.fused, head.unfused, cmp_steps, args.warmup, world)
     workloads[HEADLINE] = {
         "fused": {"ms": ms, "tflops": per_launch_tflops, "gbs": head.alg_bytes / (ms * 1e-3) / 1e9},
-        "unfused_chain": {"ms": unf_ms, "launches": 3, "extra_hbm_bytes": head.unfused_extra},
+        "unfused_chain": {"ms": unf_ms, "launches": 3, "extra_hbm_bytes": head.unfused_extra,
+                          "fused_ms_same_windows": f_cmp_ms,
+                          "timing": f"medians of 3 alternating blocks of {cmp_steps} calls, fused then unfused"},
         "roofline": roofline("tensor", per_launch_tflops, peaks["bf16_tflops"], "TFLOP/s",
                              kernel_traffic(HEADLINE)),
     }
@@ -638,13 +654,13 @@ def main():
                      "residual_layernorm_f16_16384x4096", "conv3x3_tiny_1x16x16x8_to16"]:
             r = Runner(name, seed=rank)
             steps = args.sub_steps if r.w.kind != "conv" or r.w.conv.M > 1000 else 10 * args.sub_steps
-            f_ms, _ = time_loop(r.fused, steps, args.warmup, world)
-            u_ms, _ = time_loop(r.unfused, steps // 2, args.warmup, world)
+            f_ms, u_ms = time_alternating(r.fused, r.unfused, steps, args.warmup, world)
             gbs = r.alg_bytes / (f_ms * 1e-3) / 1e9
             entry = {"fused": {"ms": f_ms, "gbs": gbs, "alg_bytes": r.alg_bytes},
                      "unfused_chain": {"ms": u_ms, "gbs_of_fused_bytes": r.alg_bytes / (u_ms * 1e-3) / 1e9,
                                        "extra_hbm_bytes": r.unfused_extra},
-                     "l2": f"{r.nsets} rotating buffer sets"}
+                     "l2": f"{r.nsets} rotating buffer sets",
+                     "timing": f"medians of 3 alternating blocks of {steps} calls, fused then unfused"}
             if r.flops:
                 entry["fused"]["tflops"] = r.flops / (f_ms * 1e-3) / 1e12
             if rank == 0 and world == 1 and not args.no_cpu_baseline:
