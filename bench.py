@@ -671,6 +671,16 @@ def main():
                 entry["unfused_chain"]["graph_us_per_call"] = graph_time_us(r.unfused, 200)
             else:
                 entry["roofline"] = roofline("hbm", gbs, peaks["hbm_gbs"], "GB/s", kernel_traffic(name))
+            if r.flops and name != HEADLINE and not name.startswith("conv3x3_tiny"):
+                # a conv below the ridge point: its share of the dense tensor peak
+                # next to its share of what the HBM roofline allows at its
+                # arithmetic intensity, min(peak, flops/bytes * bandwidth)
+                tflops = r.flops / (f_ms * 1e-3) / 1e12
+                attainable = min(peaks["bf16_tflops"], r.flops / r.alg_bytes * peaks["hbm_gbs"] / 1e3)
+                entry["tensor"] = {"tflops": round(tflops, 2), "frac_of_tensor_peak": round(tflops / peaks["bf16_tflops"], 4),
+                                   "flop_per_byte": round(r.flops / r.alg_bytes, 1),
+                                   "attainable_tflops": round(attainable, 1),
+                                   "frac_of_attainable": round(tflops / attainable, 4)}
             workloads[name] = entry
             del r
             torch.cuda.empty_cache()
