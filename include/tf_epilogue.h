@@ -110,8 +110,10 @@ int tf_pack_filter_nhwc(const void *w_oihw, void *w_ohwi,
  *   y      : bf16 NHWC [N][Ho][Wo][C_out]
  * y[n][oh][ow][co] = SiLU(acc*scale[co] + bias[co]) with
  * acc = sum_{kh,kw,ci} x[n][oh*sh-ph+kh][ow*sw-pw+kw][ci] * w[co][kh][kw][ci]
- * accumulated in fp32.  Requires C_in % 8 == 0 and 16-byte aligned x, w, y.
- * The kernel is chosen by shape (see tf_conv2d_bn_silu_select). */
+ * accumulated in fp32.  Requires C_in % 8 == 0 and 16-byte aligned x, w, y;
+ * shapes that go to a tensor-core kernel also need 16-byte aligned scale and
+ * bias (TF_ERR_UNSUPPORTED otherwise).  The kernel is chosen by shape (see
+ * tf_conv2d_bn_silu_select). */
 int tf_conv2d_bn_silu(const void *x, const void *w_ohwi, const float *scale, const float *bias,
                       void *y, const tf_conv_shape *shape, tf_stream_t stream);
 
@@ -265,15 +267,18 @@ int tf_unfused_affine(const void *nrm, const float *gamma, const float *beta, vo
 
 /* ---------------------------------------------------------------- device waits */
 
-/* Every spin-wait inside the library's kernels (mbarrier waits of the
- * tcgen05 pipeline) gives up after this many nanoseconds of %globaltimer,
- * records TF_DEVERR_* in a device error word and lets the kernel finish
- * cleanly.  Default 2e9 (2 s).  Host-side setting, applies to later launches. */
+/* Every spin-wait inside the library's kernels (the mbarrier waits of the
+ * tcgen05 pipeline and of the bulk-copy rings, and the cluster LayerNorm's
+ * wait for its peers' partial sums) gives up after this many nanoseconds of
+ * %globaltimer, records TF_DEVERR_* in a device error word and lets the
+ * kernel finish cleanly.  Default 2e9 (2 s).  Host-side setting, applies to
+ * later launches. */
 void tf_set_wait_limit_ns(uint64_t limit_ns);
 uint64_t tf_get_wait_limit_ns(void);
 
 /* Bits of the device error word. */
-#define TF_DEVERR_PRODUCER_WAIT 0x1u  /* TMA producer: smem stage never freed */
+#define TF_DEVERR_PRODUCER_WAIT 0x1u  /* conv TMA producer: a stage never freed; bulk-copy
+                                        rings (bias + GELU, LayerNorm): a stage never filled */
 #define TF_DEVERR_MMA_WAIT 0x2u       /* MMA issuer: operands or accumulator never ready */
 #define TF_DEVERR_EPILOGUE_WAIT 0x4u  /* epilogue: accumulator never committed */
 #define TF_DEVERR_DRAIN_WAIT 0x8u     /* in-flight copies/MMAs not drained on exit */
