@@ -138,62 +138,98 @@ __global__ void __launch_bounds__(kThreads) bias_gelu_kernel(const uint4 *__rest
     }
 }
 
-// Rows of up to 16384 columns: persistent CTAs of 512 threads walk chunks of
-// whole rows (at most 32 KB), chunk c, c + gridDim.x, ...  Thread 0 streams
-// the coming chunks of x into a shared-memory ring with 1-D bulk copies; the
-// threads compute GELU(x + bias) in place and thread 0 writes the chunk back
-// with a bulk store, so both directions move through the copy engine and the
-// SMs issue only the arithmetic.  A chunk holds whole rows, so thread t's
-// vectors t + 512k always have the same columns: their bias stays in
-// registers.  Waits are bounded; after a time-out the CTA stops, drains its
-// copies and records the error.
+// Rows of up to 16384 columns: persistent CTAs walk chunks of whole rows (at
+// most 32 KB), chunk c, c + gridDim.x, ...  A 17th warp, the copy warp,
+// streams the coming chunks of x into a 3-stage shared-memory ring with 1-D
+// bulk copies and writes each computed chunk back with a bulk store, so both
+// directions move through the copy engine; the 16 compute warps compute
+// GELU(x + bias) in place.  Compute warps and copy warp meet only at two
+// mbarriers per stage (loaded; computed by all 16 warps), never at a CTA-wide
+// barrier, and a stage is refilled as soon as its store has read it (5% faster
+// than one thread of a compute warp doing the copies between two CTA
+// barriers per chunk).  A chunk holds whole rows, so thread t's vectors
+// t + 512k always have the same columns: their bias stays in registers.
+// Waits are bounded; after a time-out the warps stop, the copy warp drains
+// its copies and the error is recorded.
 constexpr int kRingThreads = 512;
 constexpr int kRingVecs = 4;                       // vectors per thread per chunk: 512 * 4 * 16 B = 32 KB
 constexpr int kRingChunkBytes = kRingThreads * kRingVecs * 16;
 
-__global__ void __launch_bounds__(kRingThreads, 2) bias_gelu_ring_kernel(const uint4 *__restrict__ x,
-                                                                        const uint4 *__restrict__ bias,
-                                                                        uint4 *__restrict__ y, int64_t rows,
-                                                                        int cvec, int rps, int stages,
-                                                                        uint32_t *err, uint64_t wait_ns)
+constexpr int kRingBlock = kRingThreads + 32;   // 16 compute warps + 1 copy warp
+
+__global__ void __launch_bounds__(kRingBlock, 2) bias_gelu_ring_kernel(const uint4 *__restrict__ x,
+                                                                      const uint4 *__restrict__ bias,
+                                                                      uint4 *__restrict__ y, int64_t rows,
+                                                                      int cvec, int rps, int stages,
+                                                                      uint32_t *err, uint64_t wait_ns)
 {
     pdl_begin();
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * kRingChunkBytes);
+    uint64_t *done = full + stages;   // a stage's chunk computed in place by all 16 warps
     const int64_t nchunks = (rows + rps - 1) / rps;
     const int64_t G = gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto chunk_bytes = [&](int64_t c) -> uint32_t {
         const int64_t r = rows - c * rps < rps ? rows - c * rps : rps;
         return (uint32_t)(r * cvec * 16);
     };
-    auto issue = [&](int st, int64_t c) {
-        const uint32_t bytes = chunk_bytes(c);
-        ptx::mbar_arrive_expect_tx(&full[st], bytes);
-        ptx::bulk_load(smem + (size_t)st * kRingChunkBytes, x + c * rps * cvec, bytes, &full[st]);
-    };
-    int issued_until = 0;   // this CTA's chunks 0 .. issued_until-1 had loads issued
-    if (threadIdx.x == 0) {
-        for (int st = 0; st < stages; ++st) ptx::mbar_init(&full[st], 1);
-        ptx::mbar_init_fence();
+    if (threadIdx.x == kRingThreads) {
         for (int st = 0; st < stages; ++st) {
-            const int64_t c = blockIdx.x + st * G;
-            if (c >= nchunks) break;
-            issue(st, c);
-            issued_until = st + 1;
+            ptx::mbar_init(&full[st], 1);
+            ptx::mbar_init(&done[st], kRingThreads / 32);
         }
+        ptx::mbar_init_fence();
+    }
+    __syncthreads();
+    if (warp == kRingThreads / 32) {
+        // the copy warp: loads into free stages, stores computed ones
+        if (lane != 0) return;
+        auto issue = [&](int st, int64_t c) {
+            const uint32_t bytes = chunk_bytes(c);
+            ptx::mbar_arrive_expect_tx(&full[st], bytes);
+            ptx::bulk_load(smem + (size_t)st * kRingChunkBytes, x + c * rps * cvec, bytes, &full[st]);
+        };
+        int issued = 0;   // chunks of this CTA whose loads were issued
+        for (int st = 0; st < stages; ++st) {
+            if (blockIdx.x + st * G >= nchunks) break;
+            issue(st, blockIdx.x + st * G);
+            issued = st + 1;
+        }
+        int it = 0;
+        for (int64_t c = blockIdx.x; c < nchunks; c += G, ++it) {
+            const int st = it % stages;
+            if (!ptx::mbar_wait(&done[st], (uint32_t)(it / stages) & 1u, wait_ns)) {
+                atomicOr(err, TF_DEVERR_PRODUCER_WAIT);
+                break;
+            }
+            ptx::bulk_store(y + c * rps * cvec, smem + (size_t)st * kRingChunkBytes, chunk_bytes(c));
+            ptx::bulk_commit_group();
+            const int64_t next = c + (int64_t)stages * G;
+            if (next < nchunks) {
+                ptx::bulk_wait_group_read<0>();   // the store has read the stage: refill it
+                issue(st, next);
+                issued = it + stages + 1;
+            }
+        }
+        ptx::bulk_wait_group_all();   // every store has written y
+        // loads issued for chunks never computed (only after a time-out) land before exit
+        for (int k = it; k < issued; ++k)
+            if (!ptx::mbar_wait(&full[k % stages], (uint32_t)(k / stages) & 1u, wait_ns))
+                atomicOr(err, TF_DEVERR_DRAIN_WAIT);
+        return;
     }
     float b[kRingVecs][8];
 #pragma unroll
     for (int k = 0; k < kRingVecs; ++k) h8_to_f(__ldg(bias + (threadIdx.x + k * kRingThreads) % cvec), b[k]);
-    __syncthreads();
 
     int it = 0;
     for (int64_t c = blockIdx.x; c < nchunks; c += G, ++it) {
         const int st = it % stages;
-        const bool ok = ptx::mbar_wait(&full[st], (uint32_t)(it / stages) & 1u, wait_ns);
-        if (!__syncthreads_and(ok)) {
-            if (threadIdx.x == 0) atomicOr(err, TF_DEVERR_PRODUCER_WAIT);
-            break;
+        // one decision per warp, so that no lane leaves its warp-mates in a warp collective
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full[st], (uint32_t)(it / stages) & 1u, wait_ns))) {
+            if (lane == 0) atomicOr(err, TF_DEVERR_PRODUCER_WAIT);
+            break;   // the copy warp's wait for this chunk then runs out too
         }
         uint4 *buf = reinterpret_cast<uint4 *>(smem + (size_t)st * kRingChunkBytes);
         const int nv = (int)(chunk_bytes(c) / 16);
@@ -214,27 +250,8 @@ __global__ void __launch_bounds__(kRingThreads, 2) bias_gelu_ring_kernel(const u
             buf[v] = o;
         }
         ptx::fence_proxy_async_smem();   // the generic-proxy writes, before the bulk store reads them
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            ptx::bulk_store(y + c * rps * cvec, buf, chunk_bytes(c));
-            ptx::bulk_commit_group();
-            // refill the previous chunk's stage once its store has read it
-            if (it > 0) {
-                const int64_t next = c - G + (int64_t)stages * G;
-                if (next < nchunks) {
-                    ptx::bulk_wait_group_read<1>();
-                    issue((it - 1) % stages, next);
-                    issued_until = it - 1 + stages + 1;
-                }
-            }
-        }
-    }
-    if (threadIdx.x == 0) {
-        ptx::bulk_wait_group_all();   // every store has written y
-        // loads issued for chunks never consumed (only after a time-out) land before exit
-        for (int k = it; k < issued_until; ++k)
-            if (!ptx::mbar_wait(&full[k % stages], (uint32_t)(k / stages) & 1u, wait_ns))
-                atomicOr(err, TF_DEVERR_DRAIN_WAIT);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&done[st]);
     }
 }
 
@@ -383,19 +400,19 @@ cudaError_t launch_bias_gelu(const void *x, const void *bias, void *y, int64_t r
         if (!err) return cudaErrorInitializationError;
         const int rps = (int)(kRingChunkBytes / (cols * 2));
         const int stages = 3;
-        const size_t smem = (size_t)stages * kRingChunkBytes + 8 * stages;
+        const size_t smem = (size_t)stages * kRingChunkBytes + 16 * stages;
         cudaError_t e = cudaFuncSetAttribute(bias_gelu_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bias_gelu_ring_kernel, kRingThreads, smem) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bias_gelu_ring_kernel, kRingBlock, smem) !=
                 cudaSuccess ||
             per_sm < 1)
             per_sm = 1;
         const int64_t nchunks = (rows + rps - 1) / rps;
         int64_t grid = (int64_t)sm_count() * per_sm;
         if (grid > nchunks) grid = nchunks;
-        return launch_pdl(bias_gelu_ring_kernel, dim3((unsigned)grid), dim3(kRingThreads), smem, st,
+        return launch_pdl(bias_gelu_ring_kernel, dim3((unsigned)grid), dim3(kRingBlock), smem, st,
                           reinterpret_cast<const uint4 *>(x), reinterpret_cast<const uint4 *>(bias),
                           reinterpret_cast<uint4 *>(y), rows, (int)cvec, rps, stages, err, wait_limit_ns());
     }

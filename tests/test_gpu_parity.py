@@ -268,7 +268,10 @@ def _rowsum_check(rs_gpu, y_ref):
     assert np.all(err <= bound), f"worst row error {err.max():.4g} (bound {bound[err.argmax()]:.4g})"
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 8), (3, 200), (37, 1032), (300, 16384), (8192, 8192)])
+# Widths across the tile kernel's row-tile shapes, ragged row counts, one
+# row, two rows, and fewer row tiles than SMs.
+@pytest.mark.parametrize("rows,cols", [(1, 8), (3, 200), (37, 1032), (300, 16384), (8192, 8192),
+                                       (1000, 256), (129, 768), (77, 2048), (5, 16384), (2, 256)])
 def test_bias_gelu_rowsum_fused(b, rows, cols):
     d = synth.bias_gelu_inputs(rows, cols, seed=10)
     y = torch.empty((rows, cols), dtype=torch.float16, device="cuda")

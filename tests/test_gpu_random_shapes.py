@@ -80,6 +80,23 @@ def test_bias_gelu_random_width(b, rows, cols):
     assert ulp.max() <= 2
 
 
+@pytest.mark.parametrize("rows,cols", _random_widths(6, seed=9, hi=16384)
+                         + [(r, 256 * (c // 256 + 1)) for r, c in _random_widths(6, seed=10, hi=16000)])
+def test_bias_gelu_rowsum_random_width(b, rows, cols):
+    # half the widths multiples of 256, half arbitrary multiples of 8
+    d = synth.bias_gelu_inputs(rows, cols, seed=43)
+    y = torch.empty((rows, cols), dtype=torch.float16, device="cuda")
+    rs = torch.full((rows,), float("nan"), dtype=torch.float32, device="cuda")
+    b.tf_bias_gelu_rowsum(dev_f16(d["x"]), dev_f16(d["bias"]), y, rs, rows, cols)
+    torch.cuda.synchronize()
+    ref_y, _ = oracle.bias_gelu_rowsum(d["x"], d["bias"])
+    assert f16_ulp_distance(y.cpu().numpy().view(np.uint16), ref_y).max() <= 2
+    err = np.abs(rs.cpu().numpy().astype(np.float64) - ref_y.sum(axis=1))
+    assert np.all(err <= 1e-3 * np.abs(ref_y).sum(axis=1) + 1e-3)
+    rc, word = b.tf_read_device_error()
+    assert rc == b.TF_OK and word == 0
+
+
 @pytest.mark.parametrize("rows,hidden", _random_widths(12, seed=8, hi=48000))
 def test_layernorm_random_width_every_strategy(b, rows, hidden):
     d = synth.layernorm_inputs(rows, hidden, seed=42)
