@@ -8,6 +8,8 @@
 // the NHWC input for one filter tap straight into shared memory (zero fill at
 // the padding), which is the TMA_LOAD_IM2COL -> UMMA path that page describes;
 // a 1x1 stride-1 unpadded convolution is a plain matrix, loaded as a 2-D tile.
+// A CTA's tile is 128 output pixels, or 256 (wide tiles: two 128-row MMAs per
+// K step on one B stage).
 //
 // Persistent kernel, one CTA (or, with CL = 2, one CTA pair) per SM, with
 // 2 + EPI warps:
@@ -16,7 +18,8 @@
 //           alone when the filter block is resident)
 //   warp 1  TMEM allocator and MMA issuer: tcgen05.mma M=128, N=BN, K=16, fp32
 //           accumulators in TMEM, double-buffered so the epilogue of one tile
-//           overlaps the main loop of the next
+//           overlaps the main loop of the next (single for the 256 x 256
+//           accumulator of a wide tile, which fills TMEM)
 //   warps 2.. epilogue ("Fusing an Epilogue", "The shape of it"), 16 warps for
 //           short K loops and 8 for long ones: TMEM -> registers,
 //           v = acc*scale[co] + bias[co], v*sigmoid(v), bf16, then a swizzled
@@ -54,10 +57,14 @@ constexpr int kABytes = BM * BK * 2;          // one A (im2col) tile of a K step
 constexpr int kNumBars = 2 * kMaxStages + 5;  // full, empty, tmem full x2, tmem empty x2, drain
 constexpr int kBarBytes = kNumBars * 8 + 16;  // + the TMEM address slot
 
-template <int BN>
+// MH: 128-row halves per CTA tile (1, or 2 for 256-row tiles whose two MMAs
+// per K step share one B stage).  The fp32 accumulator of a tile takes MH*BN
+// TMEM columns; two of them (double buffering) when they fit in the 512.
+template <int BN, int MH = 1>
 struct Tile {
     static constexpr int B_BYTES = BN * BK * 2;   // one B (filter) tile of a K step
-    static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+    static constexpr int NACC = 2 * MH * BN <= 512 ? 2 : 1;
+    static constexpr uint32_t TMEM_COLS = NACC * MH * BN < 32 ? 32 : NACC * MH * BN;
 };
 
 // Shared-memory plan, from the 1024-byte-aligned base (operand tiles use
@@ -107,12 +114,20 @@ struct UmmaParams {
 // instead of re-reading the filters from L2 for every tile.  The host
 // launches a multiple of num_n_tiles CTAs, so CTA c always gets channel tile
 // c % num_n_tiles.
-template <int BN, bool IM2COL, int CL, int kEpiWarps>
+//
+// Wide tiles (MH = 2): each CTA's tile is 256 output pixels, two 128-row
+// MMAs per K step reading the same B stage, so every SM moves 64 KB of
+// operands per 1024 tensor cycles instead of 48 KB per 512.  Their 256 x BN
+// accumulator fills TMEM at BN = 256, so it is single-buffered: the MMAs of a
+// tile wait for the epilogue of the previous one, a short pause against a
+// long K loop.  Items from split_from on are then the 128-row halves of the
+// last, partial wave's tiles (parts = 2).
+template <int BN, bool IM2COL, int CL, int kEpiWarps, int MH = 1>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     conv_umma_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_y, const UmmaParams p)
 {
-    using T = Tile<BN>;
+    using T = Tile<BN, MH>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.sm.off_bar);
@@ -171,33 +186,48 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 // K step kb's B tile lands in its resident slot on the same
                 // barrier as that step's A tile
                 const bool first = work == cid;
+                const int part = work < p.split_from ? -1 : (work - p.split_from) % p.parts;
                 const int tile = work < p.split_from ? work / p.splits
                                                      : p.split_from + (work - p.split_from) / p.parts;
                 const int kb_begin = work < p.split_from ? (work - tile * p.splits) * p.kb_per_split : 0;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
-                const int m0 = ((tile / p.num_n_tiles) * CL + crank) * BM;
+                const int mh = MH > 1 && part >= 0 ? 1 : MH;   // 128-row halves this item loads
+                const int m0 = ((tile / p.num_n_tiles) * CL + crank) * (BM * MH) + (MH > 1 && part > 0 ? part * BM : 0);
                 const int n0 = (tile % p.num_n_tiles) * BN;
-                const int img = m0 / p.HoWo;
-                const int rem = m0 - img * p.HoWo;
-                const int oh = rem / p.Wo, ow = rem - (rem / p.Wo) * p.Wo;
-                const int w_base = ow * p.stride_w - p.pad_w, h_base = oh * p.stride_h - p.pad_h;
+                int img[MH], w_base[MH], h_base[MH];
+#pragma unroll
+                for (int hh = 0; hh < MH; ++hh) {
+                    const int mr = m0 + hh * BM;
+                    img[hh] = mr / p.HoWo;
+                    const int rem = mr - img[hh] * p.HoWo;
+                    const int oh = rem / p.Wo, ow = rem - (rem / p.Wo) * p.Wo;
+                    w_base[hh] = ow * p.stride_w - p.pad_w;
+                    h_base[hh] = oh * p.stride_h - p.pad_h;
+                }
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
                         ok = false;
                         break;
                     }
                     ptx::mbar_arrive_expect_tx(&full[stage],
-                                               (uint32_t)(p.sm.stage_bytes + (b_res && first ? T::B_BYTES : 0)));
+                                               (uint32_t)(p.sm.stage_bytes - (MH - mh) * kABytes +
+                                                          (b_res && first ? T::B_BYTES : 0)));
                     uint8_t *a_dst = smem + stage * p.sm.stage_bytes;
-                    uint8_t *b_dst = a_dst + kABytes;
+                    uint8_t *b_dst = a_dst + MH * kABytes;
                     const int tap = kb / p.cblocks;
                     const int c0 = (kb - tap * p.cblocks) * BK;
-                    if constexpr (IM2COL) {
-                        const int kh = tap / p.KW, kw = tap - (tap / p.KW) * p.KW;
-                        ptx::tma_load_im2col_4d(a_dst, &tmap_a, &full[stage], c0, w_base, h_base, img,
-                                                (uint16_t)kw, (uint16_t)kh);
-                    } else {
-                        ptx::tma_load_2d(a_dst, &tmap_a, &full[stage], c0, m0);
+                    for (int hh = 0; hh < mh; ++hh) {
+                        if constexpr (IM2COL) {
+                            const int kh = tap / p.KW, kw = tap - (tap / p.KW) * p.KW;
+                            ptx::tma_load_im2col_4d(a_dst + hh * kABytes, &tmap_a, &full[stage], c0, w_base[hh],
+                                                    h_base[hh], img[hh], (uint16_t)kw, (uint16_t)kh);
+                        } else {
+                            // rows past M are never stored: a box lying wholly past M (the second
+                            // CTA of a pair, a wide tile's half) starts at the last row instead, so
+                            // that every tiled load overlaps the tensor
+                            ptx::tma_load_2d(a_dst + hh * kABytes, &tmap_a, &full[stage], c0,
+                                             min(m0 + hh * BM, p.M - 1));
+                        }
                     }
                     if constexpr (CL > 1)
                         ptx::tma_load_2d_multicast(b_dst + crank * (BN / CL) * (BK * 2), &tmap_b, &full[stage],
@@ -235,17 +265,19 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 const int kb_begin = work < p.split_from ? (work % p.splits) * p.kb_per_split : 0;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
                 // part j of a tile: N = BN/parts on rows [j*BN/parts, +BN/parts) of the resident block
+                // (MH = 1), or its 128-row half j (MH = 2)
                 const int part = work < p.split_from ? -1 : (work - p.split_from) % p.parts;
-                const uint32_t id = part < 0 ? idesc : (p.parts == 2 ? idesc_half : idesc_quarter);
-                const uint32_t b_half = part > 0 ? (uint32_t)(part * (BN / p.parts)) * (BK * 2) : 0u;
-                const int b = local & 1;
-                const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
+                const int mh = MH > 1 && part >= 0 ? 1 : MH;
+                const uint32_t id = MH > 1 || part < 0 ? idesc : (p.parts == 2 ? idesc_half : idesc_quarter);
+                const uint32_t b_half = MH == 1 && part > 0 ? (uint32_t)(part * (BN / p.parts)) * (BK * 2) : 0u;
+                const int b = T::NACC == 2 ? local & 1 : 0;
+                const uint32_t acc_phase = T::NACC == 2 ? (uint32_t)(local >> 1) & 1u : (uint32_t)local & 1u;
                 if (!ptx::mbar_wait(&tempty[b], acc_phase ^ 1u, p.wait_ns)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(b * MH * BN);
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!ptx::mbar_wait(&full[stage], phase, p.wait_ns)) {
                         ok = false;
@@ -254,12 +286,15 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                     ptx::tc_fence_after();
                     const uint32_t a_addr = ptx::smem_u32(smem + stage * p.sm.stage_bytes);
                     const uint32_t b_addr = b_res ? ptx::smem_u32(smem + p.sm.off_bres + kb * T::B_BYTES) + b_half
-                                                  : a_addr + kABytes;
+                                                  : a_addr + MH * kABytes;
+                    for (int hh = 0; hh < mh; ++hh) {
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k) {
-                        ptx::umma_bf16(d_tmem, ptx::sw128_kmajor_desc(a_addr + k * UMMA_K * 2),
-                                       ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2), id,
-                                       (kb > kb_begin || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            ptx::umma_bf16(d_tmem + (uint32_t)(hh * BN),
+                                           ptx::sw128_kmajor_desc(a_addr + hh * kABytes + k * UMMA_K * 2),
+                                           ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2), id,
+                                           (kb > kb_begin || k > 0) ? 1u : 0u);
+                        }
                     }
                     // frees the stage (in every CTA of the cluster) once these MMAs have read it
                     if constexpr (CL > 1)
@@ -302,12 +337,14 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             const int part = work < p.split_from ? -1 : (work - p.split_from) % p.parts;
             const int tile = part < 0 ? work / p.splits : p.split_from + (work - p.split_from) / p.parts;
             const int split = part < 0 ? work - tile * p.splits : 0;
-            const int width = part < 0 ? BN : BN / p.parts;   // channels of this item
-            const int m0 = ((tile / p.num_n_tiles) * CL + crank) * BM;
-            const int n0 = (tile % p.num_n_tiles) * BN + (part > 0 ? part * width : 0);
-            const int b = local & 1;
-            const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-            const int slice_key = 8 * n0 + (part < 0 ? 0 : p.parts);   // the channels and width the slice must hold
+            const bool npart = MH == 1 && part >= 0;          // a part along the channels
+            const int mh = MH > 1 && part >= 0 ? 1 : MH;     // 128-row halves of this item
+            const int width = npart ? BN / p.parts : BN;       // channels of this item
+            const int m0 = ((tile / p.num_n_tiles) * CL + crank) * (BM * MH) + (MH > 1 && part > 0 ? part * BM : 0);
+            const int n0 = (tile % p.num_n_tiles) * BN + (npart && part > 0 ? part * width : 0);
+            const int b = T::NACC == 2 ? local & 1 : 0;
+            const uint32_t acc_phase = T::NACC == 2 ? (uint32_t)(local >> 1) & 1u : (uint32_t)local & 1u;
+            const int slice_key = 8 * n0 + (npart ? p.parts : 0);   // the channels and width the slice must hold
             if (p.epilogue == 1 && slice_key != slice_n0) {   // before the accumulator wait, which hides the latency
                 float sv[kChunks], bv[kChunks];
 #pragma unroll
@@ -332,56 +369,59 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 break;
             }
             ptx::tc_fence_after();
-            const int prow = m0 + q * 32;   // first pixel of this warp's rows
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
 #pragma unroll 1
-            for (int c = h, ci = 0; c * 32 < width; c += kEpiWarps / 4, ++ci) {
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
-                if (p.epilogue == 2) {
-                    // split-K partial: this lane's row, 32 fp32 channels, 128 contiguous bytes
+            for (int hh = 0; hh < mh; ++hh) {
+                const int prow = m0 + hh * BM + q * 32;   // first pixel of this warp's rows
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * MH * BN + hh * BN);
+#pragma unroll 1
+                for (int c = h, ci = 0; c * 32 < width; c += kEpiWarps / 4, ++ci) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
+                    if (p.epilogue == 2) {
+                        // split-K partial: this lane's row, 32 fp32 channels, 128 contiguous bytes
+                        ptx::tmem_ld_wait();
+                        const int m = prow + lane;
+                        if (m < p.M) {
+                            float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)split * p.M + m) * p.C_out + n0 + c * 32);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                        }
+                        continue;
+                    }
+                    // the store issued from this box for the previous chunk must have read it
+                    if (lane == 0) ptx::bulk_wait_group_read<0>();
+                    __syncwarp();
                     ptx::tmem_ld_wait();
-                    const int m = prow + lane;
-                    if (m < p.M) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)split * p.M + m) * p.C_out + n0 + c * 32);
+                    const float4 *s4 = reinterpret_cast<const float4 *>(slice + ci * 64);
+                    const float4 *b4 = reinterpret_cast<const float4 *>(slice + ci * 64 + 32);
+                    uint32_t wq[4];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    for (int j = 0; j < 8; ++j) {
+                        float2 v0 = make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]));
+                        float2 v1 = make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                        if (p.epilogue) {
+                            const float4 a4 = s4[j], c4 = b4[j];
+                            v0 = silu_f32x2(ffma2(v0, make_float2(a4.x, a4.y), make_float2(c4.x, c4.y)));
+                            v1 = silu_f32x2(ffma2(v1, make_float2(a4.z, a4.w), make_float2(c4.z, c4.w)));
+                        }
+                        __nv_bfloat162 t0 = __floats2bfloat162_rn(v0.x, v0.y), t1 = __floats2bfloat162_rn(v1.x, v1.y);
+                        wq[2 * (j & 1)] = *reinterpret_cast<uint32_t *>(&t0);
+                        wq[2 * (j & 1) + 1] = *reinterpret_cast<uint32_t *>(&t1);
+                        if (j & 1) {
+                            // row `lane`, 16-byte chunk j/2 lands at chunk (j/2) ^ ((lane >> 1) & 3):
+                            // the 64-byte swizzle the store's tensor map expects
+                            const int pj = (j >> 1) ^ ((lane >> 1) & 3);
+                            *reinterpret_cast<uint4 *>(box + lane * 64 + pj * 16) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                        }
                     }
-                    continue;
-                }
-                // the store issued from this box for the previous chunk must have read it
-                if (lane == 0) ptx::bulk_wait_group_read<0>();
-                __syncwarp();
-                ptx::tmem_ld_wait();
-                const float4 *s4 = reinterpret_cast<const float4 *>(slice + ci * 64);
-                const float4 *b4 = reinterpret_cast<const float4 *>(slice + ci * 64 + 32);
-                uint32_t wq[4];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float2 v0 = make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]));
-                    float2 v1 = make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                    if (p.epilogue) {
-                        const float4 a4 = s4[j], c4 = b4[j];
-                        v0 = silu_f32x2(ffma2(v0, make_float2(a4.x, a4.y), make_float2(c4.x, c4.y)));
-                        v1 = silu_f32x2(ffma2(v1, make_float2(a4.z, a4.w), make_float2(c4.z, c4.w)));
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (prow < p.M) ptx::tma_store_2d(&tmap_y, box, n0 + c * 32, prow);
+                        ptx::bulk_commit_group();
                     }
-                    __nv_bfloat162 t0 = __floats2bfloat162_rn(v0.x, v0.y), t1 = __floats2bfloat162_rn(v1.x, v1.y);
-                    wq[2 * (j & 1)] = *reinterpret_cast<uint32_t *>(&t0);
-                    wq[2 * (j & 1) + 1] = *reinterpret_cast<uint32_t *>(&t1);
-                    if (j & 1) {
-                        // row `lane`, 16-byte chunk j/2 lands at chunk (j/2) ^ ((lane >> 1) & 3):
-                        // the 64-byte swizzle the store's tensor map expects
-                        const int pj = (j >> 1) ^ ((lane >> 1) & 3);
-                        *reinterpret_cast<uint4 *>(box + lane * 64 + pj * 16) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-                    }
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (prow < p.M) ptx::tma_store_2d(&tmap_y, box, n0 + c * 32, prow);
-                    ptx::bulk_commit_group();
                 }
             }
             ptx::tc_fence_before();
@@ -456,16 +496,16 @@ int upper_corner(int in, int out, int stride, int pad) { return (out - 1) * stri
 // Shared-memory plan for BN x EPI: the resident filter block when asked for
 // and within kBResMaxBytes with at least 3 A stages left, else the plain
 // ring; as many stages as fit, up to kMaxStages.  False if fewer than two fit.
-template <int BN, int EPI>
+template <int BN, int EPI, int MH = 1>
 bool plan_smem(int num_kb, bool want_bres, SmemPlan &sm)
 {
     constexpr int kFixed = EPI * (kOutBoxBytes + chunks_per_warp(BN, EPI) * kParamChunkBytes) + kBarBytes +
                            1024;   // + alignment slack
     constexpr int b_bytes = Tile<BN>::B_BYTES;
     const int64_t bres_bytes = (int64_t)num_kb * b_bytes;
-    sm.b_res = want_bres && bres_bytes <= kBResMaxBytes &&
+    sm.b_res = MH == 1 && want_bres && bres_bytes <= kBResMaxBytes &&
                (kSmemLimit - kFixed - bres_bytes) / kABytes >= 3;
-    sm.stage_bytes = kABytes + (sm.b_res ? 0 : b_bytes);
+    sm.stage_bytes = MH * kABytes + (sm.b_res ? 0 : b_bytes);
     const int64_t room = kSmemLimit - kFixed - (sm.b_res ? bres_bytes : 0);
     sm.stages = (int)(room / sm.stage_bytes);
     if (sm.stages > kMaxStages) sm.stages = kMaxStages;
@@ -478,13 +518,36 @@ bool plan_smem(int num_kb, bool want_bres, SmemPlan &sm)
     return sm.alloc <= kSmemLimit;
 }
 
-template <int BN, bool IM2COL, int CL, int EPI>
+// The last, partial wave of wide tiles as their 128-row halves over twice the
+// units (CTAs, or CTA pairs), when that still fits in one wave.
+inline void split_wide_tail(UmmaParams &p, int units)
+{
+    const int rem = p.num_tiles % units;
+    if (rem > 0 && 2 * rem <= units) {
+        p.split_from = p.num_tiles - rem;
+        p.parts = 2;
+        p.num_work = p.split_from + 2 * rem;
+    }
+}
+
+template <int BN, bool IM2COL, int CL, int EPI, int MH = 1>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty, UmmaParams p,
                       bool want_bres, cudaStream_t st)
 {
     constexpr int kThreads = threads_for(EPI);
-    auto kern = conv_umma_kernel<BN, IM2COL, CL, EPI>;
-    if (!plan_smem<BN, EPI>(p.num_kb, want_bres && CL == 1 && p.splits == 1, p.sm)) return cudaErrorNotSupported;
+    auto kern = conv_umma_kernel<BN, IM2COL, CL, EPI, MH>;
+    if constexpr (MH > 1) {   // 256-row tiles: one K split, no channel parts
+        if (p.splits != 1) return cudaErrorNotSupported;
+        const int64_t mtiles = ((int64_t)p.M + BM * MH - 1) / (BM * MH);
+        p.num_tiles = (int)((mtiles + CL - 1) / CL) * p.num_n_tiles;
+        p.num_work = p.num_tiles;
+        p.split_from = p.num_work;
+        p.parts = 1;
+    }
+    // the channel tiles must cover C_out exactly: no filter box or parameter
+    // read past the last channel
+    if (p.num_n_tiles * BN != p.C_out) return cudaErrorNotSupported;
+    if (!plan_smem<BN, EPI, MH>(p.num_kb, want_bres && CL == 1 && p.splits == 1, p.sm)) return cudaErrorNotSupported;
     // Per-function, per-device attribute; cheap enough to set on every launch.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.sm.alloc);
     if (e != cudaSuccess) return e;
@@ -508,7 +571,8 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         // the last, partial wave of tiles as quarter or half tiles over 4 or 2
         // times the CTAs, when that still fits in one wave (resident block,
         // one channel tile; measured 2-2.5% off the 1x1 workload's time)
-        if (p.sm.b_res && p.num_n_tiles == 1 && p.splits == 1 && BN >= 64) {
+        if (MH > 1) split_wide_tail(p, grid);
+        if (MH == 1 && p.sm.b_res && p.num_n_tiles == 1 && p.splits == 1 && BN >= 64) {
             const int rem = p.num_tiles % grid;
             for (int parts : {4, 2}) {
                 if (rem > 0 && parts * rem <= grid && BN / parts >= 32) {
@@ -537,6 +601,7 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
         if (e != cudaSuccess) return e;
         if (clusters < 1) return cudaErrorNotSupported;
+        if (MH > 1) split_wide_tail(p, clusters);
         if (clusters > p.num_work) clusters = p.num_work;
         cfg.gridDim = dim3(CL * clusters);
         return cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
@@ -609,7 +674,10 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     EncodeTiledFn tiled = encode_tiled();
     if (!tiled) return cudaErrorNotSupported;
     const int cl = a.cluster == 2 ? 2 : 1;
-    const int bn = choose_bn(s, a.splits > 1 ? a.splits : 1, cl);
+    // wide (256-row) tiles: CTA pairs, 256-channel tiles whatever the K
+    // length (the kernel is built for BN = 256), no K split
+    if (a.wide && (cl != 2 || pick_bn(s.C_out) != 256 || a.splits > 1)) return cudaErrorNotSupported;
+    const int bn = a.wide ? 256 : choose_bn(s, a.splits > 1 ? a.splits : 1, cl);
     const int64_t M = (int64_t)s.N * a.Ho * a.Wo;
     const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
 
@@ -694,6 +762,9 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     p.parts = 1;
     if (p.err == nullptr) return cudaErrorInitializationError;
     const bool want_bres = cl == 1 && p.splits == 1;
+    if (a.wide)
+        return im2col ? launch_bn<256, true, 2, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st)
+                      : launch_bn<256, false, 2, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st);
     if (cl == 2)
         return im2col ? launch_im<true, 2>(bn, ta, tb, ty, p, false, st) : launch_im<false, 2>(bn, ta, tb, ty, p, false, st);
     return im2col ? launch_im<true, 1>(bn, ta, tb, ty, p, want_bres, st)

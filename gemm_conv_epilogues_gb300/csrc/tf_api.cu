@@ -114,8 +114,14 @@ int select_variant(const tf_conv_shape &s, int Ho, int Wo)
     const int64_t M = (int64_t)s.N * Ho * Wo;
     const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
     const double flops = 2.0 * (double)M * s.C_out * (double)K;
-    if (conv_umma_supports(s, Ho, Wo) && !(K <= 64 && flops < 10.0e6))
-        return K > 1024 && M >= 2 * 128 * (int64_t)sm_count() ? TF_CONV_UMMA_PAIR : TF_CONV_UMMA;
+    if (conv_umma_supports(s, Ho, Wo) && !(K <= 64 && flops < 10.0e6)) {
+        const int64_t sms = sm_count();
+        if (K <= 1024 || M < 2 * 128 * sms) return TF_CONV_UMMA;
+        // long reductions over at least two waves of tiles: CTA pairs; with
+        // 256-channel tiles and two waves of 512-pixel pair tiles, wide tiles
+        const int64_t wide_tiles = (M + 511) / 512 * (s.C_out / 256);
+        return s.C_out % 256 == 0 && wide_tiles >= 2 * (sms / 2) ? TF_CONV_UMMA_PAIR_WIDE : TF_CONV_UMMA_PAIR;
+    }
     const double taps = (double)M * s.C_out * s.KH * s.KW;
     if (M >= 16384 || (s.C_in <= 16 && taps >= 2.0e6)) return TF_CONV_TILED;
     return TF_CONV_DIRECT;
@@ -136,9 +142,12 @@ int run_conv(const void *x, const void *w, const float *scale, const float *bias
     case TF_CONV_TILED: return from_cuda(launch_conv_tiled(a, st));
     case TF_CONV_UMMA:
     case TF_CONV_UMMA_PAIR:
+    case TF_CONV_UMMA_PAIR_WIDE:
         if (!conv_umma_supports(*shape, Ho, Wo)) return TF_ERR_UNSUPPORTED;
+        if (variant == TF_CONV_UMMA_PAIR_WIDE && shape->C_out % 256 != 0) return TF_ERR_UNSUPPORTED;
         if (epilogue && (!aligned16(scale) || !aligned16(bias))) return TF_ERR_UNSUPPORTED;
-        a.cluster = variant == TF_CONV_UMMA_PAIR ? 2 : 1;
+        a.cluster = variant == TF_CONV_UMMA ? 1 : 2;
+        a.wide = variant == TF_CONV_UMMA_PAIR_WIDE;
         return from_cuda(launch_conv_umma(a, st));
     default: return TF_ERR_INVALID_ARG;
     }
@@ -213,7 +222,7 @@ int tf_conv2d_bn_silu(const void *x, const void *w_ohwi, const float *scale, con
 int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *scale, const float *bias, void *y,
                               const tf_conv_shape *shape, int variant, tf_stream_t stream)
 {
-    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA_PAIR) return TF_ERR_INVALID_ARG;
+    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA_PAIR_WIDE) return TF_ERR_INVALID_ARG;
     return run_conv(x, w_ohwi, scale, bias, y, shape, variant, 1, (cudaStream_t)stream);
 }
 
@@ -291,7 +300,7 @@ int tf_residual_layernorm_select(int64_t hidden)
 int tf_unfused_conv2d(const void *x, const void *w_ohwi, void *t1, const tf_conv_shape *shape, int variant,
                       tf_stream_t stream)
 {
-    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA_PAIR) return TF_ERR_INVALID_ARG;
+    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA_PAIR_WIDE) return TF_ERR_INVALID_ARG;
     return run_conv(x, w_ohwi, nullptr, nullptr, t1, shape, variant, 0, (cudaStream_t)stream);
 }
 

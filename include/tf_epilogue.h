@@ -63,9 +63,14 @@ typedef enum {
     TF_CONV_DIRECT = 0,  /* one output element per thread, CUDA-core fp32 */
     TF_CONV_TILED = 1,   /* output-space tiles with a shared-memory halo, CUDA cores */
     TF_CONV_UMMA = 2,    /* implicit GEMM: TMA im2col -> tcgen05.mma -> TMEM -> fused epilogue */
-    TF_CONV_UMMA_PAIR = 3 /* the same on 2-CTA clusters: vertically adjacent output tiles share
-                             each filter tile, loaded half by each CTA and multicast to both;
-                             the dispatch's choice for long reductions over many tiles */
+    TF_CONV_UMMA_PAIR = 3, /* the same on 2-CTA clusters: vertically adjacent output tiles share
+                              each filter tile, loaded half by each CTA and multicast to both;
+                              the dispatch's choice for long reductions (K > 1024) over at least
+                              two waves of tiles */
+    TF_CONV_UMMA_PAIR_WIDE = 4 /* CTA pairs with 256-pixel tiles per CTA: two MMAs per K step
+                                  read each filter tile (C_out % 256 == 0 only); the dispatch's
+                                  choice over TF_CONV_UMMA_PAIR when that leaves at least two
+                                  waves of these tiles */
 } tf_conv_variant;
 
 /* Row-reduction strategies of the LayerNorm kernels (see
@@ -120,7 +125,7 @@ int tf_conv2d_bn_silu(const void *x, const void *w_ohwi, const float *scale, con
 /* Same as tf_conv2d_bn_silu with the kernel forced (TF_CONV_*).  Returns
  * TF_ERR_UNSUPPORTED when the forced kernel cannot take the shape
  * (TF_CONV_UMMA and TF_CONV_UMMA_PAIR need C_in % 64 == 0, C_out % 32 == 0,
- * strides <= 8 and padding <= 128). */
+ * strides <= 8 and padding <= 128; TF_CONV_UMMA_PAIR_WIDE also C_out % 256 == 0). */
 int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *scale,
                               const float *bias, void *y, const tf_conv_shape *shape,
                               int variant, tf_stream_t stream);

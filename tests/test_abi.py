@@ -117,7 +117,9 @@ def test_dispatch_selects_by_shape(native_lib):
     sel = lambda c: b.tf_conv2d_bn_silu_select(b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad))
     assert sel(w["conv3x3_tiny_1x16x16x8_to16"].conv) == b.TF_CONV_DIRECT
     assert sel(w["conv1x1_32x56x56x256_to256"].conv) == b.TF_CONV_UMMA
-    assert sel(w["conv7x7_16x64x64x512_to512"].conv) == b.TF_CONV_UMMA_PAIR   # long K, many tiles
+    assert sel(w["conv7x7_16x64x64x512_to512"].conv) == b.TF_CONV_UMMA_PAIR_WIDE   # long K, many 256-channel tiles
+    assert sel(synth.ConvShape(16, 64, 64, 512, 128, 7, 7, (1, 1), (3, 3))) == b.TF_CONV_UMMA_PAIR   # 128 channels
+    assert sel(synth.ConvShape(1, 64, 64, 512, 256, 7, 7, (1, 1), (3, 3))) == b.TF_CONV_UMMA   # too few tiles
     # shapes the tensor-core kernel cannot take go to the CUDA-core kernels
     assert sel(synth.ConvShape(16, 32, 32, 24, 48, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
     assert sel(synth.ConvShape(4, 32, 32, 8, 64, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED

@@ -118,6 +118,7 @@ UMMA_SHAPES = [
     synth.ConvShape(4, 56, 57, 64, 512, 1, 1, (1, 1), (0, 0)),      # 2 channel tiles, several tiles per CTA
     synth.ConvShape(4, 41, 41, 64, 96, 3, 3, (1, 1), (1, 1)),       # 3 channel tiles of 32, several tiles per CTA
     synth.ConvShape(1, 12, 12, 64, 256, 3, 3, (1, 1), (1, 1)),      # short K, block too big: 128-wide tiles, streamed
+    synth.ConvShape(1, 15, 20, 64, 64, 1, 1, (1, 1), (0, 0)),       # plain GEMM, 3 tiles: a pair's second tile wholly past M
 ]
 
 
@@ -129,6 +130,51 @@ def test_conv_umma_small(b, c, variant):
     ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
     _conv_check(got, ref)
     _assert_no_device_error(b)
+
+
+# 256-pixel tiles per CTA on CTA pairs (C_out % 256 == 0).  With fewer tiles
+# than pairs every tile runs as its two 128-row halves (the tail split); the
+# second CTA's halves of a pair can lie past M.
+WIDE_SHAPES = [
+    synth.ConvShape(1, 20, 20, 64, 256, 3, 3, (1, 1), (1, 1)),      # one pair tile, halves partly past M
+    synth.ConvShape(2, 28, 28, 128, 512, 3, 3, (1, 1), (1, 1)),     # 2 channel tiles, ragged M
+    synth.ConvShape(1, 30, 30, 2048, 256, 1, 1, (1, 1), (0, 0)),    # plain GEMM, 32 K blocks
+    synth.ConvShape(1, 16, 16, 64, 256, 7, 7, (1, 1), (3, 3)),      # 7x7 pad 3
+    synth.ConvShape(2, 17, 17, 64, 256, 3, 3, (2, 2), (1, 1)),      # stride 2
+    synth.ConvShape(1, 10, 30, 128, 256, 1, 1, (1, 1), (0, 0)),     # plain GEMM, short K: a half wholly past M
+]
+
+
+@pytest.mark.parametrize("c", WIDE_SHAPES, ids=lambda c: f"{c.N}x{c.H}x{c.W}x{c.C_in}-{c.C_out}k{c.KH}s{c.stride[0]}")
+def test_conv_umma_wide_small(b, c):
+    d = synth.conv_inputs(c, seed=16, w_dist="normal_fanin")
+    got = _run_conv(b, c, d, b.TF_CONV_UMMA_PAIR_WIDE)
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    _conv_check(got, ref)
+    _assert_no_device_error(b)
+
+
+def test_conv_umma_wide_two_waves_sampled(b):
+    # 65536 pixels, 256 channels: 128 pair tiles over the GPU's pairs, a full
+    # wave and a partial one too large to split into halves
+    c = synth.ConvShape(16, 64, 64, 64, 256, 3, 3, (1, 1), (1, 1))
+    d = synth.conv_inputs(c, seed=17, w_dist="normal_fanin")
+    got = _run_conv(b, c, d, b.TF_CONV_UMMA_PAIR_WIDE).reshape(-1)
+    pts = conv_sample_points(c.N, c.Ho, c.Wo, c.C_out, 4000, seed=5)
+    ref = oracle.conv2d_bn_silu_points(d["x"], d["w_oihw"], d["scale"], d["bias"], pts, c.stride, c.pad)
+    _conv_check(got[pts], ref)
+    assert np.isfinite(got).all()
+    _assert_no_device_error(b)
+
+
+def test_conv_umma_wide_rejects_other_channel_counts(b):
+    c = synth.ConvShape(1, 12, 12, 64, 128, 3, 3, (1, 1), (1, 1))
+    x = torch.zeros((c.N, c.H, c.W, c.C_in), dtype=torch.int16, device="cuda")
+    w = torch.zeros((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device="cuda")
+    sc = torch.ones((c.C_out,), dtype=torch.float32, device="cuda")
+    y = torch.zeros((c.M, c.C_out), dtype=torch.int16, device="cuda")
+    rc = b.tf_conv2d_bn_silu_variant(x, w, sc, sc, y, _shape(b, c), b.TF_CONV_UMMA_PAIR_WIDE, check=False)
+    assert rc == b.TF_ERR_UNSUPPORTED
 
 
 SPLITK_SHAPES = [
@@ -177,7 +223,7 @@ def test_conv_dispatch_tiny_workload(b):
 
 # ---------------------------------------------------------------- conv, full workloads, sampled
 
-@pytest.mark.parametrize("variant", [-1, 2, 3], ids=["auto", "cta", "pair"])
+@pytest.mark.parametrize("variant", [-1, 2, 3, 4], ids=["auto", "cta", "pair", "wide"])
 @pytest.mark.parametrize("name,nrand", [("conv1x1_32x56x56x256_to256", 6000), ("conv7x7_16x64x64x512_to512", 1500)])
 def test_conv_full_workload_sampled(b, name, nrand, variant):
     w = synth.WORKLOADS[name]
