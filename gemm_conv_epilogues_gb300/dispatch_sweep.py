@@ -26,7 +26,8 @@ import torch
 from . import binding as b
 from . import synth
 
-NAMES = {b.TF_CONV_DIRECT: "direct", b.TF_CONV_TILED: "tiled", b.TF_CONV_UMMA: "umma"}
+NAMES = {b.TF_CONV_DIRECT: "direct", b.TF_CONV_TILED: "tiled", b.TF_CONV_UMMA: "umma",
+         b.TF_CONV_UMMA_PAIR: "umma pair", b.TF_CONV_UMMA_PAIR_WIDE: "umma pair, wide tiles"}
 
 
 def _time_us(fn, reps: int) -> float:
