@@ -99,13 +99,17 @@ int check_conv_shape(const tf_conv_shape *s, int *Ho, int *Wo)
 // gemm_conv_epilogues_gb300/dispatch_sweep.py (GPU time of CUDA-graph
 // replays over 108 shapes):
 //  - the tensor-core kernel wins wherever it can run, except on tiny
-//    reductions (K = C_in*KH*KW <= 64 and under 10 MFLOP), where its fixed
-//    cost (~3.7 us for one persistent wave) loses to the direct kernel;
-//  - for long reductions (K > 1024) over at least two waves of 128-pixel
-//    tiles it runs on CTA pairs that share each filter tile through TMA
+//    reductions (K = C_in*KH*KW <= 64 and under 6 MFLOP), where its fixed
+//    cost (~3.2 us for one persistent wave) ties or loses to the direct
+//    kernel;
+//  - im2col shapes with 256-channel tiles and at least a wave of 512-pixel
+//    pair tiles run wide tiles on CTA pairs (fastest or within 0.5% at each
+//    such shape, 15% ahead at 16x64x64, 64 -> 256, 3x3);
+//  - other long reductions (K > 1024) over at least two waves of 128-pixel
+//    tiles run on CTA pairs that share each filter tile through TMA
 //    multicast: half the L2 reads of B, which measured 1.5% faster over
 //    sustained runs, where the power cap sets the clock (1837 vs 1740 MHz
-//    on the 7x7 workload), and on par in short ones;
+//    on the 7x7 workload), and 1-3% slower in short ones;
 //  - among the CUDA-core kernels the tiled one wins from 16384 output pixels
 //    up, or with few input channels (<= 16) once there are at least ~2M
 //    output-channel-taps (M * C_out * KH * KW) to share each staged halo.
@@ -114,13 +118,18 @@ int select_variant(const tf_conv_shape &s, int Ho, int Wo)
     const int64_t M = (int64_t)s.N * Ho * Wo;
     const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
     const double flops = 2.0 * (double)M * s.C_out * (double)K;
-    if (conv_umma_supports(s, Ho, Wo) && !(K <= 64 && flops < 10.0e6)) {
+    if (conv_umma_supports(s, Ho, Wo) && !(K <= 64 && flops < 6.0e6)) {
         const int64_t sms = sm_count();
-        if (K <= 1024 || M < 2 * 128 * sms) return TF_CONV_UMMA;
-        // long reductions over at least two waves of tiles: CTA pairs; with
-        // 256-channel tiles and two waves of 512-pixel pair tiles, wide tiles
+        // im2col shapes with 256-channel tiles and at least a wave of 512-pixel
+        // pair tiles: wide tiles (fastest or within 0.5% at every such shape
+        // measured, short K included; plain 1x1 GEMMs keep their resident
+        // filter block)
+        const bool plain = s.KH == 1 && s.KW == 1 && s.stride_h == 1 && s.stride_w == 1 && s.pad_h == 0 &&
+                           s.pad_w == 0;
         const int64_t wide_tiles = (M + 511) / 512 * (s.C_out / 256);
-        return s.C_out % 256 == 0 && wide_tiles >= 2 * (sms / 2) ? TF_CONV_UMMA_PAIR_WIDE : TF_CONV_UMMA_PAIR;
+        if (!plain && s.C_out % 256 == 0 && wide_tiles >= sms / 2) return TF_CONV_UMMA_PAIR_WIDE;
+        // other long reductions over at least two waves of tiles: CTA pairs
+        return K > 1024 && M >= 2 * 128 * sms ? TF_CONV_UMMA_PAIR : TF_CONV_UMMA;
     }
     const double taps = (double)M * s.C_out * s.KH * s.KW;
     if (M >= 16384 || (s.C_in <= 16 && taps >= 2.0e6)) return TF_CONV_TILED;

@@ -78,7 +78,7 @@ def run(quick: bool = False):
         shape = b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad)
         reps = 20 if c.flops < 1e9 else 5
         t = {}
-        for v in (b.TF_CONV_DIRECT, b.TF_CONV_TILED, b.TF_CONV_UMMA):
+        for v in (b.TF_CONV_DIRECT, b.TF_CONV_TILED, b.TF_CONV_UMMA, b.TF_CONV_UMMA_PAIR, b.TF_CONV_UMMA_PAIR_WIDE):
             if b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v, check=False) != b.TF_OK:
                 continue
             t[NAMES[v]] = _time_us(lambda v=v: b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v), reps)
@@ -96,12 +96,17 @@ def run(quick: bool = False):
 
 
 def markdown(rows) -> str:
-    out = ["| N,H,W | C_in | C_out | k | MFLOP | direct us | tiled us | umma us | umma+splitk us | fastest | dispatch |",
-           "|---|---:|---:|---:|---:|---:|---:|---:|---:|---|---|"]
+    out = ["| N,H,W | C_in | C_out | k | MFLOP | direct us | tiled us | umma us | pair us | wide us | umma+splitk us "
+           "| fastest | dispatch | dispatch / fastest |",
+           "|---|---:|---:|---:|---:|---:|---:|---:|---:|---:|---:|---|---|---:|"]
     for r in rows:
         f = lambda k: f"{r['us'][k]:.1f}" if k in r["us"] else "-"
+        # the dispatch never uses a workspace: compare it with the best kernel that needs none
+        plain = {k: v for k, v in r["us"].items() if k != "umma+splitk"}
+        ratio = plain[r["dispatch"]] / min(plain.values()) if r["dispatch"] in plain else float("nan")
         out.append(f"| {r['N']},{r['H']},{r['W']} | {r['C_in']} | {r['C_out']} | {r['K']} | {r['mflop']:.1f} | "
-                   f"{f('direct')} | {f('tiled')} | {f('umma')} | {f('umma+splitk')} | {r['best']} | {r['dispatch']} |")
+                   f"{f('direct')} | {f('tiled')} | {f('umma')} | {f('umma pair')} | {f('umma pair, wide tiles')} | "
+                   f"{f('umma+splitk')} | {r['best']} | {r['dispatch']} | {ratio:.2f} |")
     agree = sum(r["best"] == r["dispatch"] for r in rows)
     out.append(f"\ndispatch picks the fastest kernel in {agree} of {len(rows)} shapes")
     return "\n".join(out)

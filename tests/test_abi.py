@@ -120,6 +120,9 @@ def test_dispatch_selects_by_shape(native_lib):
     assert sel(w["conv7x7_16x64x64x512_to512"].conv) == b.TF_CONV_UMMA_PAIR_WIDE   # long K, many 256-channel tiles
     assert sel(synth.ConvShape(16, 64, 64, 512, 128, 7, 7, (1, 1), (3, 3))) == b.TF_CONV_UMMA_PAIR   # 128 channels
     assert sel(synth.ConvShape(1, 64, 64, 512, 256, 7, 7, (1, 1), (3, 3))) == b.TF_CONV_UMMA   # too few tiles
+    assert sel(synth.ConvShape(16, 64, 64, 64, 256, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_UMMA_PAIR_WIDE   # short K too
+    assert sel(synth.ConvShape(16, 64, 64, 256, 256, 1, 1)) == b.TF_CONV_UMMA   # plain 1x1: resident filters
+    assert sel(synth.ConvShape(1, 16, 16, 64, 256, 1, 1)) == b.TF_CONV_UMMA   # 8.4 MFLOP: tensor cores win
     # shapes the tensor-core kernel cannot take go to the CUDA-core kernels
     assert sel(synth.ConvShape(16, 32, 32, 24, 48, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
     assert sel(synth.ConvShape(4, 32, 32, 8, 64, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
