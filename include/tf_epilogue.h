@@ -65,12 +65,12 @@ typedef enum {
     TF_CONV_UMMA = 2,    /* implicit GEMM: TMA im2col -> tcgen05.mma -> TMEM -> fused epilogue */
     TF_CONV_UMMA_PAIR = 3, /* the same on 2-CTA clusters: vertically adjacent output tiles share
                               each filter tile, loaded half by each CTA and multicast to both;
-                              the dispatch's choice for long reductions (K > 1024) over at least
-                              two waves of tiles */
+                              the dispatch's choice for other long reductions (K > 1024) over at
+                              least two waves of tiles */
     TF_CONV_UMMA_PAIR_WIDE = 4 /* CTA pairs with 256-pixel tiles per CTA: two MMAs per K step
                                   read each filter tile (C_out % 256 == 0 only); the dispatch's
-                                  choice over TF_CONV_UMMA_PAIR when that leaves at least two
-                                  waves of these tiles */
+                                  choice for im2col shapes (not plain 1x1 GEMMs) with
+                                  C_out % 256 == 0 and at least a wave of 512-pixel pair tiles */
 } tf_conv_variant;
 
 /* Row-reduction strategies of the LayerNorm kernels (see
