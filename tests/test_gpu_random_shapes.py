@@ -169,3 +169,39 @@ def test_calls_captured_in_a_cuda_graph(b):
         assert np.abs(ln_out.cpu().numpy().astype(np.float64) - ref_ln).max() <= 1e-2
     rc, word = b.tf_read_device_error()
     assert rc == b.TF_OK and word == 0
+
+
+@pytest.mark.parametrize("variant", ["pair", "wide"])
+def test_cluster_conv_captured_in_a_cuda_graph(b, variant):
+    # the CTA-pair kernels (cluster and programmatic-launch attributes)
+    # captured once and replayed on new inputs, wide tiles with their
+    # half-tile tail
+    v = b.TF_CONV_UMMA_PAIR if variant == "pair" else b.TF_CONV_UMMA_PAIR_WIDE
+    c = synth.ConvShape(2, 20, 20, 64, 256, 3, 3, (1, 1), (1, 1))
+    d0 = synth.conv_inputs(c, seed=80, w_dist="normal_fanin")
+    w = torch.empty((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device="cuda")
+    b.tf_pack_filter_nhwc(dev_u16(d0["w_oihw"]), w, c.C_out, c.C_in, c.KH, c.KW)
+    sc, bi = dev_f32(d0["scale"]), dev_f32(d0["bias"])
+    shape = b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad)
+    x = torch.empty((c.N, c.H, c.W, c.C_in), dtype=torch.int16, device="cuda")
+    y = torch.empty((c.M, c.C_out), dtype=torch.int16, device="cuda")
+    x.copy_(dev_u16(d0["x"]))
+    b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v)   # first call outside the capture
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v, stream=torch.cuda.current_stream())
+    for k in range(3):
+        d = synth.conv_inputs(c, seed=81 + k, w_dist="normal_fanin")
+        x.copy_(dev_u16(d["x"]))
+        y.fill_(0x7FC0)   # NaN sentinel: every output must be rewritten by the replay
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = oracle.conv2d_bn_silu(d["x"], d0["w_oihw"], d0["scale"], d0["bias"], c.stride, c.pad)
+        got = bf16_to_f64(host_u16(y)).reshape(ref.shape)
+        assert np.all(np.abs(got - ref) <= 1e-2 + 1e-2 * np.abs(ref))
+    rc, word = b.tf_read_device_error()
+    assert rc == b.TF_OK and word == 0
+
