@@ -15,7 +15,7 @@
  *  - Arguments are validated on the host before anything is launched:
  *      TF_ERR_INVALID_ARG  a required pointer is NULL or a size is <= 0
  *                          (or the shape has an empty output);
- *      TF_ERR_UNSUPPORTED  a layout or alignment this build has no kernel
+ *      TF_ERR_UNSUPPORTED  a layout or alignment the library has no kernel
  *                          for (e.g. a pointer not 16-byte aligned, a row
  *                          length not a multiple of 8);
  *      TF_ERR_CUDA         the CUDA runtime refused the launch;
@@ -177,7 +177,7 @@ int tf_conv2d_bn_silu_static_ws(const void *x, const void *w_ohwi, const float *
 /* The kernel tf_conv2d_bn_silu would run for this shape (host only, launches
  * nothing), or a negative tf_status value when the shape is rejected.
  * "Fusing an Epilogue", "Three kernels for one operation": the lowering picks
- * one of three kernels by shape with hand-chosen thresholds; this build's
+ * one of three kernels by shape with hand-chosen thresholds; this library's
  * thresholds are measured on GB300. */
 int tf_conv2d_bn_silu_select(const tf_conv_shape *shape);
 
