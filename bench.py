@@ -561,16 +561,20 @@ def run_reference(args, world, rank):
         cpu_baseline_conv7x7(target_s=min(step_s, 1.0))
     for _ in range(args.steps):
         per_step.append(cpu_baseline_conv7x7(target_s=step_s))
+    print(json.dumps(reference_line(per_step, args.gpus, args.steps, args.warmup)), flush=True)
+
+
+def reference_line(per_step, gpus, steps, warmup) -> dict:
+    """The reference arm's JSON line from its timed oracle samples."""
     v = statistics.median(p["value"] for p in per_step)
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup,
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": gpus,
+            "steps": steps, "warmup": warmup,
             "ms_per_step": statistics.median(p["seconds"] for p in per_step) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": HEADLINE, "note": "bounded sample per step"},
             "cpu_baseline": {"kind": "oracle", "cores": per_step[0]["cores"], "sample": per_step[0]["sample"],
                              "value": v, "unit": "TFLOP/s"},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
 
 
 def main():
