@@ -317,7 +317,9 @@ int tf_unfused_bn(const void *t1, const float *scale, const float *bias, void *t
                   tf_stream_t stream)
 {
     if (!t1 || !scale || !bias || !t2 || bad_rows_cols(M, C)) return TF_ERR_INVALID_ARG;
-    if (C % 8 != 0 || !aligned16(t1) || !aligned16(t2)) return TF_ERR_UNSUPPORTED;
+    // scale and bias are read as 16-byte vectors
+    if (C % 8 != 0 || !aligned16(t1) || !aligned16(t2) || !aligned16(scale) || !aligned16(bias))
+        return TF_ERR_UNSUPPORTED;
     return from_cuda(launch_unfused_bn(t1, scale, bias, t2, M, C, (cudaStream_t)stream));
 }
 
@@ -361,7 +363,9 @@ int tf_unfused_affine(const void *nrm, const float *gamma, const float *beta, vo
                       tf_stream_t stream)
 {
     if (!nrm || !gamma || !beta || !y || bad_rows_cols(rows, hidden)) return TF_ERR_INVALID_ARG;
-    if (hidden % 8 != 0 || !aligned16(nrm) || !aligned16(y)) return TF_ERR_UNSUPPORTED;
+    // gamma and beta are read as 16-byte vectors
+    if (hidden % 8 != 0 || !aligned16(nrm) || !aligned16(y) || !aligned16(gamma) || !aligned16(beta))
+        return TF_ERR_UNSUPPORTED;
     return from_cuda(launch_unfused_affine(nrm, gamma, beta, y, rows, hidden, (cudaStream_t)stream));
 }
 

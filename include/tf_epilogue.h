@@ -245,7 +245,8 @@ int tf_residual_layernorm_select(int64_t hidden);
  * tf_conv2d_bn_silu_variant. */
 int tf_unfused_conv2d(const void *x, const void *w_ohwi, void *t1, const tf_conv_shape *shape,
                       int variant, tf_stream_t stream);
-/* t2[m][c] = t1[m][c]*scale[c] + bias[c]; bf16 [M][C], C % 8 == 0. */
+/* t2[m][c] = t1[m][c]*scale[c] + bias[c]; bf16 [M][C], C % 8 == 0, all four
+ * pointers 16-byte aligned. */
 int tf_unfused_bn(const void *t1, const float *scale, const float *bias, void *t2,
                   int64_t M, int64_t C, tf_stream_t stream);
 /* y = t2 * sigmoid(t2); bf16, n % 8 == 0. */
@@ -266,7 +267,8 @@ int tf_unfused_residual_add(const void *act, const void *res, void *s, int64_t n
  * (hidden <= 131072, same strategies as tf_residual_layernorm). */
 int tf_unfused_layernorm(const void *s, void *nrm, int64_t rows, int64_t hidden, float eps,
                          tf_stream_t stream);
-/* y[i][j] = nrm[i][j]*gamma[j] + beta[j]; fp16 in and out, fp32 gamma/beta. */
+/* y[i][j] = nrm[i][j]*gamma[j] + beta[j]; fp16 in and out, fp32 gamma/beta;
+ * all four pointers 16-byte aligned. */
 int tf_unfused_affine(const void *nrm, const float *gamma, const float *beta, void *y,
                       int64_t rows, int64_t hidden, tf_stream_t stream);
 

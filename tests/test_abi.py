@@ -94,6 +94,14 @@ def test_host_validation_rejects_before_launch(native_lib):
     assert b.tf_unfused_residual_add(p16, p16, p16, 12, 0, check=False) == U
     assert b.tf_unfused_layernorm(p16, p16, 2, 10, 1e-5, 0, check=False) == U
     assert b.tf_unfused_affine(p16, p16, p16, None, 2, 8, 0, check=False) == S
+    # per-channel parameters read as 16-byte vectors must be aligned
+    quad = p16 + 4   # 4-byte aligned, as a float array can be
+    assert b.tf_unfused_bn(p16, quad, p16, p16, 4, 8, 0, check=False) == U
+    assert b.tf_unfused_bn(p16, p16, quad, p16, 4, 8, 0, check=False) == U
+    assert b.tf_unfused_affine(p16, quad, p16, p16, 2, 8, 0, check=False) == U
+    assert b.tf_unfused_affine(p16, p16, quad, p16, 2, 8, 0, check=False) == U
+    assert b.tf_unfused_bias_add(p16, odd, p16, 2, 8, 0, check=False) == U
+    assert b.tf_residual_layernorm(p16, p16, quad, p16, p16, 4, 64, 1e-5, 0, check=False) == U
 
 
 def test_split_k_workspace_size(native_lib):
