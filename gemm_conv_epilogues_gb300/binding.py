@@ -15,7 +15,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libtf_epilogue.so")
 
 TF_OK, TF_ERR_INVALID_ARG, TF_ERR_UNSUPPORTED, TF_ERR_CUDA, TF_ERR_TIMEOUT = 0, 1, 2, 3, 4
-TF_CONV_AUTO, TF_CONV_DIRECT, TF_CONV_TILED, TF_CONV_UMMA, TF_CONV_UMMA_PAIR, TF_CONV_UMMA_PAIR_WIDE = -1, 0, 1, 2, 3, 4
+(TF_CONV_AUTO, TF_CONV_DIRECT, TF_CONV_TILED, TF_CONV_UMMA, TF_CONV_UMMA_PAIR, TF_CONV_UMMA_PAIR_WIDE,
+ TF_CONV_UMMA_WIDE) = -1, 0, 1, 2, 3, 4, 5
 TF_LN_AUTO, TF_LN_WARP, TF_LN_CTA, TF_LN_CLUSTER = -1, 0, 1, 2
 TF_DEVERR_PRODUCER_WAIT, TF_DEVERR_MMA_WAIT, TF_DEVERR_EPILOGUE_WAIT = 0x1, 0x2, 0x4
 TF_DEVERR_DRAIN_WAIT, TF_DEVERR_PROBE_WAIT, TF_DEVERR_EXCHANGE_WAIT = 0x8, 0x10, 0x20

@@ -60,9 +60,9 @@ constexpr int kBarBytes = kNumBars * 8 + 16;  // + the TMEM address slot
 // MH: 128-row halves per CTA tile (1, or 2 for 256-row tiles whose two MMAs
 // per K step share one B stage).  The fp32 accumulator of a tile takes MH*BN
 // TMEM columns; two of them (double buffering) when they fit in the 512.
-template <int BN, int MH = 1>
+template <int BN, int MH = 1, int CG = 1>
 struct Tile {
-    static constexpr int B_BYTES = BN * BK * 2;   // one B (filter) tile of a K step
+    static constexpr int B_BYTES = BN * BK * 2 / CG;   // this CTA's share of a K step's B (filter) tile
     static constexpr int NACC = 2 * MH * BN <= 512 ? 2 : 1;
     static constexpr uint32_t TMEM_COLS = NACC * MH * BN < 32 ? 32 : NACC * MH * BN;
 };
@@ -99,11 +99,10 @@ struct UmmaParams {
 };
 
 // CL: CTAs per cluster along M (1 or 2).  With CL = 2 the two CTAs of a
-// cluster take vertically adjacent output tiles that share the same filter
-// (B) tile; each loads half of B and multicasts it to both, and each MMA
-// thread's stage release is multicast to both producers, so a stage is
-// refilled only after both CTAs have consumed it.  Every SM then fetches
-// 16 KB of A + BN*64 B of B per 64-deep K step instead of 16 KB + BN*128 B.
+// cluster take vertically adjacent output tiles that read the same filter
+// (B) tile at the same time, so the second read of each B tile is an L2 hit
+// on the same GPC; each CTA loads its own operands and the two share nothing
+// else (no cross-CTA copies or barriers in the pipeline).
 //
 // Resident filter (p.sm.b_res, CL = 1 and one K split only): when the whole
 // [K][BN] filter block of the CTA's output-channel tile fits in shared memory
@@ -122,12 +121,27 @@ struct UmmaParams {
 // tile wait for the epilogue of the previous one, a short pause against a
 // long K loop.  Items from split_from on are then the 128-row halves of the
 // last, partial wave's tiles (parts = 2).
-template <int BN, bool IM2COL, int CL, int kEpiWarps, int MH = 1>
+//
+// Paired MMA (CG = 2, on CL = 2 clusters): the two CTAs of a pair run one
+// tcgen05.mma.cta_group::2 of M = 256 (128 rows per CTA, MH of them per K
+// step) issued by the first CTA.  Each CTA loads its own A rows and HALF of
+// the filter tile (BN/2 rows), and the tensor cores of both SMs read both
+// halves: the pair shares B without any copy between the CTAs.  Every SM then
+// moves 16 KB of A + BN*64 B of B per 64-deep K step (BN = 256: 32 KB per
+// 512 tensor cycles), and its accumulator is 128 x BN, so at BN = 256 two of
+// them still fit in TMEM (double buffering).  Both CTAs' copies complete on
+// the first CTA's `full` barrier (.cta_group::2 loads), the first CTA's MMA
+// commits release the stages and hand over the accumulators in both CTAs,
+// and both CTAs' epilogue warps report a drained accumulator to the first
+// CTA's `tempty` barrier.
+template <int BN, bool IM2COL, int CL, int kEpiWarps, int MH = 1, int CG = 1>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     conv_umma_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_y, const UmmaParams p)
 {
-    using T = Tile<BN, MH>;
+    static_assert(CG == 1 || CL == 2, "a paired MMA runs on a 2-CTA cluster");
+    constexpr bool PAIR = CG == 2;
+    using T = Tile<BN, MH, CG>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.sm.off_bar);
@@ -142,15 +156,18 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int crank = CL > 1 ? (int)ptx::cluster_ctarank() : 0;
     const int cid = (int)blockIdx.x / CL, ncl = (int)gridDim.x / CL;   // cluster index and count
+    const bool leader = !PAIR || crank == 0;   // the CTA whose thread issues the (paired) MMAs
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], CL);   // released by the MMA thread of every CTA of the cluster
+            ptx::mbar_init(&empty[s], 1);    // released by this CTA's MMA thread
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&tfull[b], 1);
-            ptx::mbar_init(&tempty[b], kEpiWarps * 32);
+            // every epilogue thread arrives; with a paired MMA, one lane per
+            // epilogue warp of either CTA arrives on the first CTA's barrier
+            ptx::mbar_init(&tempty[b], PAIR ? 2 * kEpiWarps : kEpiWarps * 32);
         }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init_fence();
@@ -159,13 +176,20 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         ptx::prefetch_tensormap(&tmap_y);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(tmem_slot, T::TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(tmem_slot, T::TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(tmem_slot, T::TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if constexpr (CL > 1) ptx::cluster_sync();   // peers' barriers exist before any multicast
+    // a pair's barriers exist in both CTAs before any copy, commit or arrival
+    // from the other CTA reaches them
+    if constexpr (PAIR) ptx::cluster_sync();
     // The set-up above touched no global memory; from here on the kernel
     // reads and writes it, so it waits for the stream's previous kernel
     // (programmatic dependent launch), and lets the next one start its own
@@ -173,6 +197,15 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
+    int num_work = p.num_work;
+    if constexpr (PAIR) {
+        // the paired MMA writes both CTAs' accumulators at the first CTA's
+        // TMEM address: if the two allocations differ, no work is done
+        if (ptx::ld_shared_cluster_u32(ptx::mapa_shared(tmem_slot, (uint32_t)crank ^ 1u)) != tmem_base) {
+            num_work = 0;
+            if (threadIdx.x == 0) atomicOr(p.err, TF_DEVERR_PAIR_TMEM);
+        }
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -181,7 +214,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             uint32_t phase = 0;
             uint32_t issued = 0, last_phase = 0;  // per-stage bit masks
             bool ok = true;
-            for (int work = cid; ok && work < p.num_work; work += ncl) {
+            for (int work = cid; ok && work < num_work; work += ncl) {
                 // a resident filter block streams in with the CTA's first tile:
                 // K step kb's B tile lands in its resident slot on the same
                 // barrier as that step's A tile
@@ -209,9 +242,12 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(&full[stage],
-                                               (uint32_t)(p.sm.stage_bytes - (MH - mh) * kABytes +
-                                                          (b_res && first ? T::B_BYTES : 0)));
+                    // bytes this CTA loads for the stage; with a paired MMA both CTAs
+                    // load as much, and all of it completes on the first CTA's barrier
+                    const uint32_t own = (uint32_t)(p.sm.stage_bytes - (MH - mh) * kABytes +
+                                                    (b_res && first ? T::B_BYTES : 0));
+                    if (leader) ptx::mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * own : own);
+                    const uint32_t full_pair = PAIR ? ptx::mapa_shared(&full[stage], 0) : 0u;
                     uint8_t *a_dst = smem + stage * p.sm.stage_bytes;
                     uint8_t *b_dst = a_dst + MH * kABytes;
                     const int tap = kb / p.cblocks;
@@ -219,19 +255,27 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                     for (int hh = 0; hh < mh; ++hh) {
                         if constexpr (IM2COL) {
                             const int kh = tap / p.KW, kw = tap - (tap / p.KW) * p.KW;
-                            ptx::tma_load_im2col_4d(a_dst + hh * kABytes, &tmap_a, &full[stage], c0, w_base[hh],
-                                                    h_base[hh], img[hh], (uint16_t)kw, (uint16_t)kh);
+                            if constexpr (PAIR)
+                                ptx::tma_load_im2col_4d_pair(a_dst + hh * kABytes, &tmap_a, full_pair, c0,
+                                                             w_base[hh], h_base[hh], img[hh], (uint16_t)kw,
+                                                             (uint16_t)kh);
+                            else
+                                ptx::tma_load_im2col_4d(a_dst + hh * kABytes, &tmap_a, &full[stage], c0,
+                                                        w_base[hh], h_base[hh], img[hh], (uint16_t)kw,
+                                                        (uint16_t)kh);
                         } else {
                             // rows past M are never stored: a box lying wholly past M (the second
                             // CTA of a pair, a wide tile's half) starts at the last row instead, so
                             // that every tiled load overlaps the tensor
-                            ptx::tma_load_2d(a_dst + hh * kABytes, &tmap_a, &full[stage], c0,
-                                             min(m0 + hh * BM, p.M - 1));
+                            const int row = min(m0 + hh * BM, p.M - 1);
+                            if constexpr (PAIR)
+                                ptx::tma_load_2d_pair(a_dst + hh * kABytes, &tmap_a, full_pair, c0, row);
+                            else
+                                ptx::tma_load_2d(a_dst + hh * kABytes, &tmap_a, &full[stage], c0, row);
                         }
                     }
-                    if constexpr (CL > 1)
-                        ptx::tma_load_2d_multicast(b_dst + crank * (BN / CL) * (BK * 2), &tmap_b, &full[stage],
-                                                   kb * BK, n0 + crank * (BN / CL), (uint16_t)((1u << CL) - 1));
+                    if constexpr (PAIR)   // this CTA's half of the filter tile
+                        ptx::tma_load_2d_pair(b_dst, &tmap_b, full_pair, kb * BK, n0 + crank * (BN / 2));
                     else if (!b_res)
                         ptx::tma_load_2d(b_dst, &tmap_b, &full[stage], kb * BK, n0);
                     else if (first)
@@ -245,23 +289,25 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 }
             }
             if (!ok) atomicOr(p.err, TF_DEVERR_PRODUCER_WAIT);
-            // Every issued copy must have landed before the CTA may exit.
+            // Every issued copy must have landed before the CTA may exit (a
+            // pair's copies all complete on the first CTA's barriers, which its
+            // producer drains before the pair's closing cluster barrier).
             for (int s = 0; s < nstages; ++s)
-                if ((issued >> s) & 1u)
+                if (leader && ((issued >> s) & 1u))
                     if (!ptx::mbar_wait(&full[s], (last_phase >> s) & 1u, p.wait_ns))
                         atomicOr(p.err, TF_DEVERR_DRAIN_WAIT);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
             constexpr uint32_t idesc_half = ptx::idesc_bf16_f32(BM, BN / 2);
             constexpr uint32_t idesc_quarter = ptx::idesc_bf16_f32(BM, BN / 4);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int work = cid; ok && work < p.num_work; work += ncl, ++local) {
+            for (int work = cid; ok && work < num_work; work += ncl, ++local) {
                 const int kb_begin = work < p.split_from ? (work % p.splits) * p.kb_per_split : 0;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
                 // part j of a tile: N = BN/parts on rows [j*BN/parts, +BN/parts) of the resident block
@@ -272,7 +318,8 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 const uint32_t b_half = MH == 1 && part > 0 ? (uint32_t)(part * (BN / p.parts)) * (BK * 2) : 0u;
                 const int b = T::NACC == 2 ? local & 1 : 0;
                 const uint32_t acc_phase = T::NACC == 2 ? (uint32_t)(local >> 1) & 1u : (uint32_t)local & 1u;
-                if (!ptx::mbar_wait(&tempty[b], acc_phase ^ 1u, p.wait_ns)) {
+                // (cluster-scope acquire for a pair: the peer's epilogue arrives here)
+                if (!ptx::mbar_wait<PAIR>(&tempty[b], acc_phase ^ 1u, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -290,27 +337,41 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                     for (int hh = 0; hh < mh; ++hh) {
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k) {
-                            ptx::umma_bf16(d_tmem + (uint32_t)(hh * BN),
-                                           ptx::sw128_kmajor_desc(a_addr + hh * kABytes + k * UMMA_K * 2),
-                                           ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2), id,
-                                           (kb > kb_begin || k > 0) ? 1u : 0u);
+                            const uint64_t ad = ptx::sw128_kmajor_desc(a_addr + hh * kABytes + k * UMMA_K * 2);
+                            const uint64_t bd = ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2);
+                            const uint32_t acc = (kb > kb_begin || k > 0) ? 1u : 0u;
+                            if constexpr (PAIR)
+                                ptx::umma_bf16_pair(d_tmem + (uint32_t)(hh * BN), ad, bd, id, acc);
+                            else
+                                ptx::umma_bf16(d_tmem + (uint32_t)(hh * BN), ad, bd, id, acc);
                         }
                     }
-                    // frees the stage (in every CTA of the cluster) once these MMAs have read it
-                    if constexpr (CL > 1)
-                        ptx::umma_commit_multicast(&empty[stage], (uint16_t)((1u << CL) - 1));
-                    else
+                    // frees the stage (in both CTAs of a pair) once these MMAs have read it
+                    if constexpr (PAIR) {
+                        ptx::umma_commit_pair(ptx::mapa_shared(&empty[stage], 0));
+                        ptx::umma_commit_pair(ptx::mapa_shared(&empty[stage], 1));
+                    } else {
                         ptx::umma_commit(&empty[stage]);
+                    }
                     if (++stage == nstages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                ptx::umma_commit(&tfull[b]);  // accumulator complete
+                // accumulator complete (in both CTAs of a pair)
+                if constexpr (PAIR) {
+                    ptx::umma_commit_pair(ptx::mapa_shared(&tfull[b], 0));
+                    ptx::umma_commit_pair(ptx::mapa_shared(&tfull[b], 1));
+                } else {
+                    ptx::umma_commit(&tfull[b]);
+                }
             }
             if (!ok) atomicOr(p.err, TF_DEVERR_MMA_WAIT);
-            ptx::umma_commit(drain);
+            if constexpr (PAIR)
+                ptx::umma_commit_pair(ptx::smem_u32(drain));
+            else
+                ptx::umma_commit(drain);
             if (!ptx::mbar_wait(drain, 0, p.wait_ns)) atomicOr(p.err, TF_DEVERR_DRAIN_WAIT);
         }
     } else {
@@ -333,7 +394,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         int slice_n0 = -1;   // 8 * first channel + parts of the item whose parameters the slice holds
         int local = 0;
         bool ok = true;
-        for (int work = cid; work < p.num_work; work += ncl, ++local) {
+        for (int work = cid; work < num_work; work += ncl, ++local) {
             const int part = work < p.split_from ? -1 : (work - p.split_from) % p.parts;
             const int tile = part < 0 ? work / p.splits : p.split_from + (work - p.split_from) / p.parts;
             const int split = part < 0 ? work - tile * p.splits : 0;
@@ -425,7 +486,12 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 }
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&tempty[b]);
+            if constexpr (PAIR) {
+                __syncwarp();   // every lane's TMEM reads of this accumulator are done
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(&tempty[b], 0));
+            } else {
+                ptx::mbar_arrive(&tempty[b]);
+            }
         }
         if (lane == 0) ptx::bulk_wait_group_all();   // stores complete before exit
         if (!ok && lane == 0) atomicOr(p.err, TF_DEVERR_EPILOGUE_WAIT);
@@ -433,11 +499,15 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    // no CTA exits while its peer may still multicast into it or release its stages
-    if constexpr (CL > 1) ptx::cluster_sync();
+    // neither CTA of a pair frees its TMEM or exits while the pair's MMAs,
+    // commits, copies or arrivals may still reach it
+    if constexpr (PAIR) ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, T::TMEM_COLS);
+        if constexpr (PAIR)
+            ptx::tmem_dealloc_pair(tmem_base, T::TMEM_COLS);
+        else
+            ptx::tmem_dealloc(tmem_base, T::TMEM_COLS);
     }
 }
 
@@ -496,14 +566,14 @@ int upper_corner(int in, int out, int stride, int pad) { return (out - 1) * stri
 // Shared-memory plan for BN x EPI: the resident filter block when asked for
 // and within kBResMaxBytes with at least 3 A stages left, else the plain
 // ring; as many stages as fit, up to kMaxStages.  False if fewer than two fit.
-template <int BN, int EPI, int MH = 1>
+template <int BN, int EPI, int MH = 1, int CG = 1>
 bool plan_smem(int num_kb, bool want_bres, SmemPlan &sm)
 {
     constexpr int kFixed = EPI * (kOutBoxBytes + chunks_per_warp(BN, EPI) * kParamChunkBytes) + kBarBytes +
                            1024;   // + alignment slack
-    constexpr int b_bytes = Tile<BN>::B_BYTES;
+    constexpr int b_bytes = Tile<BN, MH, CG>::B_BYTES;
     const int64_t bres_bytes = (int64_t)num_kb * b_bytes;
-    sm.b_res = MH == 1 && want_bres && bres_bytes <= kBResMaxBytes &&
+    sm.b_res = MH == 1 && CG == 1 && want_bres && bres_bytes <= kBResMaxBytes &&
                (kSmemLimit - kFixed - bres_bytes) / kABytes >= 3;
     sm.stage_bytes = MH * kABytes + (sm.b_res ? 0 : b_bytes);
     const int64_t room = kSmemLimit - kFixed - (sm.b_res ? bres_bytes : 0);
@@ -530,12 +600,13 @@ inline void split_wide_tail(UmmaParams &p, int units)
     }
 }
 
-template <int BN, bool IM2COL, int CL, int EPI, int MH = 1>
+template <int BN, bool IM2COL, int CL, int EPI, int MH = 1, int CG = 1>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty, UmmaParams p,
                       bool want_bres, cudaStream_t st)
 {
     constexpr int kThreads = threads_for(EPI);
-    auto kern = conv_umma_kernel<BN, IM2COL, CL, EPI, MH>;
+    auto kern = conv_umma_kernel<BN, IM2COL, CL, EPI, MH, CG>;
+    if (CG == 2 && p.splits != 1) return cudaErrorNotSupported;   // paired MMAs: one K split
     if constexpr (MH > 1) {   // 256-row tiles: one K split, no channel parts
         if (p.splits != 1) return cudaErrorNotSupported;
         const int64_t mtiles = ((int64_t)p.M + BM * MH - 1) / (BM * MH);
@@ -547,7 +618,8 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
     // the channel tiles must cover C_out exactly: no filter box or parameter
     // read past the last channel
     if (p.num_n_tiles * BN != p.C_out) return cudaErrorNotSupported;
-    if (!plan_smem<BN, EPI, MH>(p.num_kb, want_bres && CL == 1 && p.splits == 1, p.sm)) return cudaErrorNotSupported;
+    if (!plan_smem<BN, EPI, MH, CG>(p.num_kb, want_bres && CL == 1 && p.splits == 1, p.sm))
+        return cudaErrorNotSupported;
     // Per-function, per-device attribute; cheap enough to set on every launch.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.sm.alloc);
     if (e != cudaSuccess) return e;
@@ -608,15 +680,15 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
     }
 }
 
-template <bool IM2COL, int CL, int EPI>
+template <bool IM2COL, int CL, int EPI, int CG = 1>
 cudaError_t launch_epi(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
                        const UmmaParams &p, bool want_bres, cudaStream_t st)
 {
     switch (bn) {
-    case 256: return launch_bn<256, IM2COL, CL, EPI>(ta, tb, ty, p, want_bres, st);
-    case 128: return launch_bn<128, IM2COL, CL, EPI>(ta, tb, ty, p, want_bres, st);
-    case 64: return launch_bn<64, IM2COL, CL, EPI>(ta, tb, ty, p, want_bres, st);
-    case 32: return launch_bn<32, IM2COL, CL, EPI>(ta, tb, ty, p, want_bres, st);
+    case 256: return launch_bn<256, IM2COL, CL, EPI, 1, CG>(ta, tb, ty, p, want_bres, st);
+    case 128: return launch_bn<128, IM2COL, CL, EPI, 1, CG>(ta, tb, ty, p, want_bres, st);
+    case 64: return launch_bn<64, IM2COL, CL, EPI, 1, CG>(ta, tb, ty, p, want_bres, st);
+    case 32: return launch_bn<32, IM2COL, CL, EPI, 1, CG>(ta, tb, ty, p, want_bres, st);
     default: return cudaErrorNotSupported;
     }
 }
@@ -625,24 +697,26 @@ cudaError_t launch_epi(int bn, const CUtensorMap &ta, const CUtensorMap &tb, con
 // epilogue needs for the previous tile: such kernels get more epilogue warps.
 bool short_k(int kb_per_split) { return kb_per_split <= 16; }
 
-template <bool IM2COL, int CL>
+template <bool IM2COL, int CL, int CG = 1>
 cudaError_t launch_im(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
                       const UmmaParams &p, bool want_bres, cudaStream_t st)
 {
-    if (short_k(p.kb_per_split)) return launch_epi<IM2COL, CL, kEpiWarpsShortK>(bn, ta, tb, ty, p, want_bres, st);
-    return launch_epi<IM2COL, CL, kEpiWarpsLongK>(bn, ta, tb, ty, p, want_bres, st);
+    if (short_k(p.kb_per_split))
+        return launch_epi<IM2COL, CL, kEpiWarpsShortK, CG>(bn, ta, tb, ty, p, want_bres, st);
+    return launch_epi<IM2COL, CL, kEpiWarpsLongK, CG>(bn, ta, tb, ty, p, want_bres, st);
 }
 
 // Channel tile width: the widest of 256/128/64/32 dividing C_out, except that
-// a short-K kernel (sixteen epilogue warps) takes 128 instead of 256 unless
-// its whole filter block can stay resident: at 256 only three ring stages
-// would fit beside the staging boxes.
-int choose_bn(const tf_conv_shape &s, int splits, int cl)
+// a short-K kernel (sixteen epilogue warps) on single CTAs takes 128 instead
+// of 256 unless its whole filter block can stay resident: at 256 only three
+// ring stages would fit beside the staging boxes.  (A paired MMA holds half
+// the filter tile per CTA, so 256 leaves room for five.)
+int choose_bn(const tf_conv_shape &s, int splits, int cl, bool pair_mma)
 {
     int bn = pick_bn(s.C_out);
     const int num_kb = s.KH * s.KW * s.C_in / BK;
     const int kb_per_split = (num_kb + splits - 1) / splits;
-    if (bn == 256 && short_k(kb_per_split)) {
+    if (bn == 256 && short_k(kb_per_split) && !pair_mma) {
         const bool resident = cl == 1 && splits == 1 && (int64_t)num_kb * Tile<256>::B_BYTES <= kBResMaxBytes;
         if (!resident) bn = 128;
     }
@@ -673,11 +747,14 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     if (!conv_umma_supports(s, a.Ho, a.Wo)) return cudaErrorNotSupported;
     EncodeTiledFn tiled = encode_tiled();
     if (!tiled) return cudaErrorNotSupported;
+    // a 2-CTA cluster always runs the paired MMA (each CTA holds half of B)
     const int cl = a.cluster == 2 ? 2 : 1;
-    // wide (256-row) tiles: CTA pairs, 256-channel tiles whatever the K
-    // length (the kernel is built for BN = 256), no K split
-    if (a.wide && (cl != 2 || pick_bn(s.C_out) != 256 || a.splits > 1)) return cudaErrorNotSupported;
-    const int bn = a.wide ? 256 : choose_bn(s, a.splits > 1 ? a.splits : 1, cl);
+    const bool pair = cl == 2;
+    // wide (256-row) tiles: 256-channel tiles whatever the K length (the
+    // kernel is built for BN = 256), no K split
+    if (a.wide && (pick_bn(s.C_out) != 256 || a.splits > 1)) return cudaErrorNotSupported;
+    if (pair && a.splits > 1) return cudaErrorNotSupported;
+    const int bn = a.wide ? 256 : choose_bn(s, a.splits > 1 ? a.splits : 1, cl, pair);
     const int64_t M = (int64_t)s.N * a.Ho * a.Wo;
     const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
 
@@ -692,10 +769,10 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    {   // B: packed filters as a [C_out][K] K-major matrix (each CTA of a cluster loads BN/cl rows)
+    {   // B: packed filters as a [C_out][K] K-major matrix (half a tile's rows per CTA of a pair)
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)s.C_out};
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {BK, (cuuint32_t)(bn / cl)};
+        const cuuint32_t box[2] = {BK, (cuuint32_t)(pair ? bn / 2 : bn)};
         const cuuint32_t estr[2] = {1, 1};
         if (tiled(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.w), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -762,11 +839,15 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     p.parts = 1;
     if (p.err == nullptr) return cudaErrorInitializationError;
     const bool want_bres = cl == 1 && p.splits == 1;
+    if (a.wide && pair)
+        return im2col ? launch_bn<256, true, 2, kEpiWarpsLongK, 2, 2>(ta, tb, ty, p, false, st)
+                      : launch_bn<256, false, 2, kEpiWarpsLongK, 2, 2>(ta, tb, ty, p, false, st);
     if (a.wide)
-        return im2col ? launch_bn<256, true, 2, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st)
-                      : launch_bn<256, false, 2, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st);
-    if (cl == 2)
-        return im2col ? launch_im<true, 2>(bn, ta, tb, ty, p, false, st) : launch_im<false, 2>(bn, ta, tb, ty, p, false, st);
+        return im2col ? launch_bn<256, true, 1, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st)
+                      : launch_bn<256, false, 1, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st);
+    if (pair)
+        return im2col ? launch_im<true, 2, 2>(bn, ta, tb, ty, p, false, st)
+                      : launch_im<false, 2, 2>(bn, ta, tb, ty, p, false, st);
     return im2col ? launch_im<true, 1>(bn, ta, tb, ty, p, want_bres, st)
                   : launch_im<false, 1>(bn, ta, tb, ty, p, want_bres, st);
 }

@@ -104,19 +104,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *map, uint64_t
         : "memory");
 }
 
-// 2-D tiled load multicast to the CTAs of the cluster in `mask`: the box lands
-// at the same shared-memory offset in each of them and completes `bytes` on
-// the mbarrier at the same offset in each.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const void *map, uint64_t *bar, int c0, int c1,
-                                                      uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
     uint32_t r;
@@ -140,6 +127,21 @@ __device__ __forceinline__ void st_async_f32x2(uint32_t remote_addr, float a, fl
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(remote_addr),
                  "f"(a), "f"(b), "r"(remote_bar)
                  : "memory");
+}
+
+// Arrives once on an mbarrier given by its shared::cluster address (this
+// CTA's or a peer's), with release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 32-bit load from a shared::cluster address (this CTA's or a peer's).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
 }
 
 // Programmatic dependent launch.  griddep_wait: block until the grids this
@@ -169,6 +171,30 @@ __device__ __forceinline__ void tma_load_im2col_4d(void *dst, const void *map, u
         "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(smem_u32(dst)),
         "l"(map), "r"(c), "r"(w), "r"(h), "r"(n), "r"(smem_u32(bar)), "h"(off_w), "h"(off_h)
+        : "memory");
+}
+
+// CTA-pair forms of the two loads above (.cta_group::2): the box lands in
+// this CTA's shared memory, and the completed bytes are counted on the
+// mbarrier at `bar_cluster`, a shared::cluster address that may lie in the
+// peer CTA of the pair -- so one barrier in the pair's first CTA can track
+// the operands both CTAs load for a paired MMA.
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const void *map, uint32_t bar_cluster, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_im2col_4d_pair(void *dst, const void *map, uint32_t bar_cluster, int c,
+                                                        int w, int h, int n, uint16_t off_w, uint16_t off_h)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar_cluster), "h"(off_w), "h"(off_h)
         : "memory");
 }
 
@@ -242,6 +268,27 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// CTA-pair forms (.cta_group::2).  The warp with the allocator role in EACH
+// of the two CTAs of the pair executes the alloc (and later the dealloc)
+// together with its peer; the columns are allocated at the same TMEM address
+// in both CTAs, which each CTA finds in its own `slot`.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -257,6 +304,31 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// Paired MMA (.cta_group::2), issued by one thread of the pair's first CTA:
+// M = 256 rows, rows 0..127 of A read from this CTA's shared memory and rows
+// 128..255 from the peer's at the same offsets; B's N rows split likewise
+// (the first N/2 here, the rest in the peer); D rows 0..127 accumulate in this
+// CTA's TMEM and rows 128..255 in the peer's, at the same TMEM address.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives once on the mbarrier at `bar_cluster` (this CTA's or the peer's)
+// when every paired tcgen05 operation this thread has issued so far has
+// completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar_cluster)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
+
 // Arrives once on the mbarrier when every tcgen05 operation this thread has
 // issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
@@ -264,17 +336,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// Same, arriving on the mbarrier at this offset in every CTA of the cluster
-// in `mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
 }
 
 // 32 TMEM lanes x 32 consecutive 32-bit columns: lane i of the warp receives

@@ -103,13 +103,11 @@ int check_conv_shape(const tf_conv_shape *s, int *Ho, int *Wo)
 //    cost (~3.2 us for one persistent wave) ties or loses to the direct
 //    kernel;
 //  - im2col shapes with 256-channel tiles and at least a wave of 512-pixel
-//    pair tiles run wide tiles on CTA pairs (fastest or within 0.5% at each
-//    such shape, 15% ahead at 16x64x64, 64 -> 256, 3x3);
+//    pair tiles run wide tiles on CTA pairs with the paired MMA
+//    (tcgen05 cta_group::2: each CTA holds half of every filter tile and the
+//    two SMs' tensor cores read both halves);
 //  - other long reductions (K > 1024) over at least two waves of 128-pixel
-//    tiles run on CTA pairs that share each filter tile through TMA
-//    multicast: half the L2 reads of B, which measured 1.5% faster over
-//    sustained runs, where the power cap sets the clock (1837 vs 1740 MHz
-//    on the 7x7 workload), and 1-3% slower in short ones;
+//    tiles run the paired MMA on 128-pixel tiles per CTA;
 //  - among the CUDA-core kernels the tiled one wins from 16384 output pixels
 //    up, or with few input channels (<= 16) once there are at least ~2M
 //    output-channel-taps (M * C_out * KH * KW) to share each staged halo.
@@ -121,9 +119,8 @@ int select_variant(const tf_conv_shape &s, int Ho, int Wo)
     if (conv_umma_supports(s, Ho, Wo) && !(K <= 64 && flops < 6.0e6)) {
         const int64_t sms = sm_count();
         // im2col shapes with 256-channel tiles and at least a wave of 512-pixel
-        // pair tiles: wide tiles (fastest or within 0.5% at every such shape
-        // measured, short K included; plain 1x1 GEMMs keep their resident
-        // filter block)
+        // pair tiles: wide tiles on paired MMAs (plain 1x1 GEMMs keep their
+        // resident filter block)
         const bool plain = s.KH == 1 && s.KW == 1 && s.stride_h == 1 && s.stride_w == 1 && s.pad_h == 0 &&
                            s.pad_w == 0;
         const int64_t wide_tiles = (M + 511) / 512 * (s.C_out / 256);
@@ -152,11 +149,12 @@ int run_conv(const void *x, const void *w, const float *scale, const float *bias
     case TF_CONV_UMMA:
     case TF_CONV_UMMA_PAIR:
     case TF_CONV_UMMA_PAIR_WIDE:
+    case TF_CONV_UMMA_WIDE:
         if (!conv_umma_supports(*shape, Ho, Wo)) return TF_ERR_UNSUPPORTED;
-        if (variant == TF_CONV_UMMA_PAIR_WIDE && shape->C_out % 256 != 0) return TF_ERR_UNSUPPORTED;
+        a.wide = variant == TF_CONV_UMMA_PAIR_WIDE || variant == TF_CONV_UMMA_WIDE;
+        if (a.wide && shape->C_out % 256 != 0) return TF_ERR_UNSUPPORTED;
         if (epilogue && (!aligned16(scale) || !aligned16(bias))) return TF_ERR_UNSUPPORTED;
-        a.cluster = variant == TF_CONV_UMMA ? 1 : 2;
-        a.wide = variant == TF_CONV_UMMA_PAIR_WIDE;
+        a.cluster = variant == TF_CONV_UMMA_PAIR || variant == TF_CONV_UMMA_PAIR_WIDE ? 2 : 1;
         return from_cuda(launch_conv_umma(a, st));
     default: return TF_ERR_INVALID_ARG;
     }
@@ -231,7 +229,7 @@ int tf_conv2d_bn_silu(const void *x, const void *w_ohwi, const float *scale, con
 int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *scale, const float *bias, void *y,
                               const tf_conv_shape *shape, int variant, tf_stream_t stream)
 {
-    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA_PAIR_WIDE) return TF_ERR_INVALID_ARG;
+    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA_WIDE) return TF_ERR_INVALID_ARG;
     return run_conv(x, w_ohwi, scale, bias, y, shape, variant, 1, (cudaStream_t)stream);
 }
 
@@ -309,7 +307,7 @@ int tf_residual_layernorm_select(int64_t hidden)
 int tf_unfused_conv2d(const void *x, const void *w_ohwi, void *t1, const tf_conv_shape *shape, int variant,
                       tf_stream_t stream)
 {
-    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA_PAIR_WIDE) return TF_ERR_INVALID_ARG;
+    if (variant < TF_CONV_AUTO || variant > TF_CONV_UMMA_WIDE) return TF_ERR_INVALID_ARG;
     return run_conv(x, w_ohwi, nullptr, nullptr, t1, shape, variant, 0, (cudaStream_t)stream);
 }
 

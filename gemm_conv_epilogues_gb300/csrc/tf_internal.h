@@ -29,8 +29,8 @@ struct ConvArgs {
     int epilogue;
     int splits = 1;          // tensor-core kernel only: K splits, fp32 partials to ws
     float *ws = nullptr;
-    int cluster = 1;         // tensor-core kernel only: 2 = CTA pairs sharing filter tiles by multicast
-    bool wide = false;       // tensor-core kernel on CTA pairs only: 256-row tiles (two MMAs per K step)
+    int cluster = 1;         // tensor-core kernel only: 2 = CTA pairs running paired (cta_group::2) MMAs
+    bool wide = false;       // tensor-core kernel only: 256-row tiles per CTA (two MMAs per K step)
 };
 cudaError_t launch_conv_direct(const ConvArgs &a, cudaStream_t st);
 cudaError_t launch_conv_tiled(const ConvArgs &a, cudaStream_t st);

@@ -27,7 +27,8 @@ from . import binding as b
 from . import synth
 
 NAMES = {b.TF_CONV_DIRECT: "direct", b.TF_CONV_TILED: "tiled", b.TF_CONV_UMMA: "umma",
-         b.TF_CONV_UMMA_PAIR: "umma pair", b.TF_CONV_UMMA_PAIR_WIDE: "umma pair, wide tiles"}
+         b.TF_CONV_UMMA_PAIR: "umma pair", b.TF_CONV_UMMA_PAIR_WIDE: "umma pair, wide tiles",
+         b.TF_CONV_UMMA_WIDE: "umma, wide tiles"}
 
 
 def _time_us(fn, reps: int) -> float:
@@ -78,7 +79,8 @@ def run(quick: bool = False):
         shape = b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad)
         reps = 20 if c.flops < 1e9 else 5
         t = {}
-        for v in (b.TF_CONV_DIRECT, b.TF_CONV_TILED, b.TF_CONV_UMMA, b.TF_CONV_UMMA_PAIR, b.TF_CONV_UMMA_PAIR_WIDE):
+        for v in (b.TF_CONV_DIRECT, b.TF_CONV_TILED, b.TF_CONV_UMMA, b.TF_CONV_UMMA_PAIR, b.TF_CONV_UMMA_PAIR_WIDE,
+                  b.TF_CONV_UMMA_WIDE):
             if b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v, check=False) != b.TF_OK:
                 continue
             t[NAMES[v]] = _time_us(lambda v=v: b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v), reps)

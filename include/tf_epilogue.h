@@ -63,14 +63,16 @@ typedef enum {
     TF_CONV_DIRECT = 0,  /* one output element per thread, CUDA-core fp32 */
     TF_CONV_TILED = 1,   /* output-space tiles with a shared-memory halo, CUDA cores */
     TF_CONV_UMMA = 2,    /* implicit GEMM: TMA im2col -> tcgen05.mma -> TMEM -> fused epilogue */
-    TF_CONV_UMMA_PAIR = 3, /* the same on 2-CTA clusters: vertically adjacent output tiles share
-                              each filter tile, loaded half by each CTA and multicast to both;
-                              the dispatch's choice for other long reductions (K > 1024) over at
-                              least two waves of tiles */
-    TF_CONV_UMMA_PAIR_WIDE = 4 /* CTA pairs with 256-pixel tiles per CTA: two MMAs per K step
-                                  read each filter tile (C_out % 256 == 0 only); the dispatch's
-                                  choice for im2col shapes (not plain 1x1 GEMMs) with
+    TF_CONV_UMMA_PAIR = 3, /* the same on CTA pairs (2-CTA clusters) with the paired MMA
+                              (tcgen05 .cta_group::2, M = 256): each CTA loads its own 128 output
+                              pixels and HALF of every filter tile, and the two SMs' tensor cores
+                              read both halves; the dispatch's choice for other long reductions
+                              (K > 1024) over at least two waves of tiles */
+    TF_CONV_UMMA_PAIR_WIDE = 4, /* paired MMA with 256-pixel tiles per CTA: two M = 256 MMAs per K
+                                  step read each half filter tile (C_out % 256 == 0 only); the
+                                  dispatch's choice for im2col shapes (not plain 1x1 GEMMs) with
                                   C_out % 256 == 0 and at least a wave of 512-pixel pair tiles */
+    TF_CONV_UMMA_WIDE = 5  /* 256-pixel tiles on single CTAs (C_out % 256 == 0 only) */
 } tf_conv_variant;
 
 /* Row-reduction strategies of the LayerNorm kernels (see
@@ -125,7 +127,8 @@ int tf_conv2d_bn_silu(const void *x, const void *w_ohwi, const float *scale, con
 /* Same as tf_conv2d_bn_silu with the kernel forced (TF_CONV_*).  Returns
  * TF_ERR_UNSUPPORTED when the forced kernel cannot take the shape
  * (TF_CONV_UMMA and TF_CONV_UMMA_PAIR need C_in % 64 == 0, C_out % 32 == 0,
- * strides <= 8 and padding <= 128; TF_CONV_UMMA_PAIR_WIDE also C_out % 256 == 0). */
+ * strides <= 8 and padding <= 128; TF_CONV_UMMA_PAIR_WIDE and TF_CONV_UMMA_WIDE
+ * also C_out % 256 == 0). */
 int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *scale,
                               const float *bias, void *y, const tf_conv_shape *shape,
                               int variant, tf_stream_t stream);
@@ -291,6 +294,8 @@ uint64_t tf_get_wait_limit_ns(void);
 #define TF_DEVERR_DRAIN_WAIT 0x8u     /* in-flight copies/MMAs not drained on exit */
 #define TF_DEVERR_PROBE_WAIT 0x10u    /* tf_wait_probe: the expected time-out */
 #define TF_DEVERR_EXCHANGE_WAIT 0x20u /* cluster LayerNorm: a peer CTA's partial sum never arrived */
+#define TF_DEVERR_PAIR_TMEM 0x40u     /* paired conv MMA: the two CTAs' TMEM allocations differ
+                                         (the pair did no work) */
 
 /* Synchronises the current device, copies the device error word of the
  * current device into *word (may be NULL), clears it, and returns TF_OK if it

@@ -145,10 +145,11 @@ WIDE_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("variant", [4, 5], ids=["pair", "cta"])
 @pytest.mark.parametrize("c", WIDE_SHAPES, ids=lambda c: f"{c.N}x{c.H}x{c.W}x{c.C_in}-{c.C_out}k{c.KH}s{c.stride[0]}")
-def test_conv_umma_wide_small(b, c):
+def test_conv_umma_wide_small(b, c, variant):
     d = synth.conv_inputs(c, seed=16, w_dist="normal_fanin")
-    got = _run_conv(b, c, d, b.TF_CONV_UMMA_PAIR_WIDE)
+    got = _run_conv(b, c, d, variant)
     ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
     _conv_check(got, ref)
     _assert_no_device_error(b)
