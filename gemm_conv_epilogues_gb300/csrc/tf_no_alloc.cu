@@ -37,7 +37,10 @@ void *static_workspace()
     std::lock_guard<std::mutex> lock(g_ws_mu);
     if (!g_ws_ptr[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess) {
+            cudaGetLastError();   // reported as TF_ERR_CUDA; not left pending for a later call
+            return nullptr;
+        }
         g_ws_ptr[dev] = p;
     }
     return g_ws_ptr[dev];

@@ -54,7 +54,7 @@ def test_conv_random_shape_every_kernel(b, c):
     if c.C_in % 64 == 0 and c.C_out % 32 == 0:
         variants += [b.TF_CONV_UMMA, b.TF_CONV_UMMA_PAIR]
         if c.C_out % 256 == 0:
-            variants.append(b.TF_CONV_UMMA_PAIR_WIDE)
+            variants += [b.TF_CONV_UMMA_PAIR_WIDE, b.TF_CONV_UMMA_WIDE]
     for v in variants:
         y = torch.full((c.M, c.C_out), 0x7FC0, dtype=torch.int16, device="cuda")   # NaN sentinel
         b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v)
