@@ -480,6 +480,13 @@ def copy_reference_gbs(nbytes: int = 1 << 30, reps: int = 20) -> float:
     return gbs
 
 
+def traffic_ratio(workload: str, alg_bytes: int):
+    """ncu DRAM bytes per launch over the algorithmic bytes (None without a
+    current capture)."""
+    t = kernel_traffic(workload)
+    return round(t / alg_bytes, 3) if t else None
+
+
 def roofline(bound, achieved, peak, unit, traffic):
     return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": traffic}
@@ -639,17 +646,21 @@ def main():
     if rc != b.TF_OK:
         raise SystemExit(f"device error word {word:#x} after the timed region")
 
+    # Every workload's numbers, compact (the full line stays short enough to be
+    # kept whole in a log tail).  Keys: ms = fused ms per call; gbs / tflops =
+    # throughput of the algorithmic bytes / flops; frac = fraction of the
+    # roofline peak named in `peaks`; dram_ratio = ncu DRAM bytes (read +
+    # write, steady state) over the algorithmic bytes; unf_ms = the unfused
+    # chain of our own kernels, timed in alternating blocks with the fused
+    # call (fused_ms_alt = the fused call in those same windows); cpu_s = the
+    # oracle on the whole workload, all host cores.
     workloads = {}
     cmp_steps = max(20, args.steps // 10)
     f_cmp_ms, unf_ms = time_alternating(head.fused, head.unfused, cmp_steps, args.warmup, world)
-    workloads[HEADLINE] = {
-        "fused": {"ms": ms, "tflops": per_launch_tflops, "gbs": head.alg_bytes / (ms * 1e-3) / 1e9},
-        "unfused_chain": {"ms": unf_ms, "launches": 3, "extra_hbm_bytes": head.unfused_extra,
-                          "fused_ms_same_windows": f_cmp_ms,
-                          "timing": f"medians of 3 alternating blocks of {cmp_steps} calls, fused then unfused"},
-        "roofline": roofline("tensor", per_launch_tflops, peaks["bf16_tflops"], "TFLOP/s",
-                             kernel_traffic(HEADLINE)),
-    }
+    head_roof = roofline("tensor", per_launch_tflops, peaks["bf16_tflops"], "TFLOP/s", kernel_traffic(HEADLINE))
+    workloads[HEADLINE] = {"ms": round(ms, 5), "tflops": round(per_launch_tflops, 1), "frac": head_roof["frac"],
+                           "dram_ratio": traffic_ratio(HEADLINE, head.alg_bytes),
+                           "unf_ms": round(unf_ms, 5), "fused_ms_alt": round(f_cmp_ms, 5)}
     del head
     torch.cuda.empty_cache()
 
@@ -660,54 +671,44 @@ def main():
             steps = args.sub_steps if r.w.kind != "conv" or r.w.conv.M > 1000 else 10 * args.sub_steps
             f_ms, u_ms = time_alternating(r.fused, r.unfused, steps, args.warmup, world)
             gbs = r.alg_bytes / (f_ms * 1e-3) / 1e9
-            entry = {"fused": {"ms": f_ms, "gbs": gbs, "alg_bytes": r.alg_bytes},
-                     "unfused_chain": {"ms": u_ms, "gbs_of_fused_bytes": r.alg_bytes / (u_ms * 1e-3) / 1e9,
-                                       "extra_hbm_bytes": r.unfused_extra},
-                     "l2": f"{r.nsets} rotating buffer sets",
-                     "timing": f"medians of 3 alternating blocks of {steps} calls, fused then unfused"}
-            if r.flops:
-                entry["fused"]["tflops"] = r.flops / (f_ms * 1e-3) / 1e12
-            if rank == 0 and world == 1 and not args.no_cpu_baseline:
-                entry["cpu_oracle"] = cpu_oracle_full(r)
+            entry = {"ms": round(f_ms, 5), "gbs": round(gbs, 1)}
             if name.startswith("conv3x3_tiny"):
-                entry["note"] = "launch-latency bound (0.59 MFLOP); reported as latency"
-                entry["fused"]["graph_us_per_call"] = graph_time_us(r.fused, 200)
-                entry["unfused_chain"]["graph_us_per_call"] = graph_time_us(r.unfused, 200)
+                # launch-latency bound (0.59 MFLOP): GPU time per call inside a CUDA graph
+                entry["graph_us"] = round(graph_time_us(r.fused, 200), 2)
+                entry["unf_graph_us"] = round(graph_time_us(r.unfused, 200), 2)
             else:
-                entry["roofline"] = roofline("hbm", gbs, peaks["hbm_gbs"], "GB/s", kernel_traffic(name))
-            if r.flops and name != HEADLINE and not name.startswith("conv3x3_tiny"):
+                entry["frac"] = round(gbs / peaks["hbm_gbs"], 4)
+                entry["dram_ratio"] = traffic_ratio(name, r.alg_bytes)
+            if r.flops and not name.startswith("conv3x3_tiny"):
                 # a conv below the ridge point: its share of the dense tensor peak
                 # next to its share of what the HBM roofline allows at its
                 # arithmetic intensity, min(peak, flops/bytes * bandwidth)
                 tflops = r.flops / (f_ms * 1e-3) / 1e12
                 attainable = min(peaks["bf16_tflops"], r.flops / r.alg_bytes * peaks["hbm_gbs"] / 1e3)
-                entry["tensor"] = {"tflops": round(tflops, 2), "frac_of_tensor_peak": round(tflops / peaks["bf16_tflops"], 4),
-                                   "flop_per_byte": round(r.flops / r.alg_bytes, 1),
-                                   "attainable_tflops": round(attainable, 1),
-                                   "frac_of_attainable": round(tflops / attainable, 4)}
+                entry.update({"tflops": round(tflops, 1), "frac_tensor": round(tflops / peaks["bf16_tflops"], 4),
+                              "frac_attainable": round(tflops / attainable, 4)})
+            entry["unf_ms"] = round(u_ms, 5)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                entry["cpu_s"] = cpu_oracle_full(r)["seconds"]
             workloads[name] = entry
             del r
             torch.cuda.empty_cache()
 
-        # the activation between two convs: in the producer's epilogue, or standalone
+        # the activation between two convs (producer 1x1 256->128, consumer 7x7
+        # 128->128 on 16x64x64): in the producer's epilogue, or as standalone
+        # BN and SiLU kernels after a plain producer conv
         pr = PairRunner(seed=rank)
         steps = max(10, args.sub_steps // 4)
         f_ms, _ = time_loop(pr.fused, steps, args.warmup, world)
         s_ms, _ = time_loop(pr.standalone, steps, args.warmup, world)
         a_ms, _ = time_loop(pr.activation, steps, args.warmup, world)
         workloads["producer_consumer_1x1_256to128_then_7x7_128to128"] = {
-            "fused_pipeline_ms": f_ms, "standalone_activation_pipeline_ms": s_ms,
-            "standalone_activation_kernels_ms": a_ms,
-            "standalone_activation_share_of_busy": a_ms / s_ms,
-            "note": "producer 1x1 conv -> BN+SiLU -> consumer 7x7 conv on 16x64x64; fused puts BN+SiLU in the "
-                    "producer's epilogue (write cardinality), standalone runs a plain producer conv then BN and "
-                    "SiLU kernels"}
+            "ms": round(f_ms, 5), "standalone_ms": round(s_ms, 5), "act_ms": round(a_ms, 5),
+            "act_share": round(a_ms / s_ms, 4)}
         del pr
         torch.cuda.empty_cache()
-        workloads["hbm_copy_reference"] = {
-            "gbs": round(copy_reference_gbs(), 1),
-            "note": "torch device-to-device copy of 1 GiB (read + write bytes / time): what a plain streaming "
-                    "copy reaches on this GPU, for context beside the memory-bound kernels"}
+        # a plain 1 GiB device-to-device copy: what streaming reaches on this GPU
+        workloads["hbm_copy_reference"] = {"gbs": round(copy_reference_gbs(), 1)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -725,17 +726,17 @@ def main():
                        "KW": 7, "stride": 1, "pad": 3, "flops_per_step_per_gpu": head_flops(),
                        "l2": "rotating input/output buffer sets, >2x L2 touched between reuses",
                        "parallelism": f"replicas x{world}"},
-            "roofline": workloads[HEADLINE]["roofline"],
-            "peak_source": peaks["source"],
+            "roofline": head_roof,
+            "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
+                      "source": peaks["source"]},
             "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(16 * 64 * 64 * 512 * 2),
                     "d2h_bytes_per_step": int(16 * 64 * 64 * 512 * 2),
-                    "mode": "copies on their own streams, overlapping the neighbouring steps' convs; "
-                            "the uploaded input is still L2-resident when the conv reads it",
+                    "mode": "copies on side streams overlap neighbouring steps",
                     "serial_value": round(e2e_serial_val, 2), "serial_ms_per_step": round(e2e_serial_ms, 5)},
             "gpu_launches": launches,
             "clocks": {"sm_mhz": cs["sm_mhz"], "sm_max_mhz": cs["sm_max_mhz"], "reasons": cs["reasons"]},
-            "workloads": workloads,
             "cpu_baseline": cpu,
+            "workloads": workloads,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -30,6 +30,7 @@
 // copies and MMAs before it frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <string.h>
 
 #include "ptx_sm100.cuh"
 #include "tf_internal.h"
@@ -40,7 +41,8 @@ namespace {
 constexpr int BM = 128;            // output pixels per tile (UMMA M)
 constexpr int BK = 64;             // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
-constexpr int kMaxStages = 6;      // deepest operand ring the shared-memory plan may choose
+constexpr int kMaxStages = 8;      // deepest operand ring the shared-memory plan may choose
+constexpr int kMaxStagesStreamed = 6;   // ... when B streams through the ring with A
 constexpr int kSmemLimit = 227 * 1024;        // opt-in dynamic shared memory per block
 constexpr int kBResMaxBytes = 128 * 1024;     // largest filter block kept resident in shared memory
 constexpr int kParamChunkBytes = 64 * 4;      // 32 scale + 32 bias floats of one 32-channel chunk
@@ -88,6 +90,8 @@ struct UmmaParams {
     int stride_h, stride_w, pad_h, pad_w;
     int num_kb, cblocks, num_n_tiles, num_tiles;
     int epilogue;            // 0: plain bf16 store, 1: BN + SiLU, 2: fp32 split-K partial to ws
+    int y_direct;            // 1: rows of y are not a multiple of 16 bytes (C_out % 8 != 0), so no
+                             // TMA store: each warp copies its staging box to y with masked stores
     int splits, kb_per_split, num_work;   // work item = (tile, K split), split fastest
     // Items from split_from on are parts of tiles (BN/parts channels each):
     // item split_from + parts*i + j is part j of tile split_from + i.  Only
@@ -104,15 +108,16 @@ struct UmmaParams {
 // on the same GPC; each CTA loads its own operands and the two share nothing
 // else (no cross-CTA copies or barriers in the pipeline).
 //
-// Resident filter (p.sm.b_res, CL = 1 and one K split only): when the whole
-// [K][BN] filter block of the CTA's output-channel tile fits in shared memory
-// (K <= 256 at BN = 256: a 1x1 convolution of up to 256 input channels) it is
+// Resident filter (p.sm.b_res, one K split only): when the whole [K][BN]
+// filter block of the CTA's output-channel tile fits in shared memory (K <=
+// 256 at BN = 256: a 1x1 convolution of up to 256 input channels; with a
+// paired MMA each CTA holds only its half of the block, so up to 512) it is
 // loaded once, K step by K step alongside the A tiles of the CTA's first
 // tile, and afterwards only A streams through the ring: a memory-bound
 // convolution then moves just its activations and outputs through each SM
-// instead of re-reading the filters from L2 for every tile.  The host
-// launches a multiple of num_n_tiles CTAs, so CTA c always gets channel tile
-// c % num_n_tiles.
+// instead of re-reading the filters from L2 for every tile, and the ring can
+// be deeper.  The host launches a multiple of num_n_tiles CTAs (or pairs), so
+// that each keeps one channel tile.
 //
 // Wide tiles (MH = 2): each CTA's tile is 256 output pixels, two 128-row
 // MMAs per K step reading the same B stage, so every SM moves 64 KB of
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     const int nstages = p.sm.stages;
-    const bool b_res = CL == 1 && p.sm.b_res != 0;
+    const bool b_res = p.sm.b_res != 0;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int crank = CL > 1 ? (int)ptx::cluster_ctarank() : 0;
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         ptx::mbar_init_fence();
         ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
-        ptx::prefetch_tensormap(&tmap_y);
+        if (!p.y_direct) ptx::prefetch_tensormap(&tmap_y);
     }
     if (warp == 1) {
         if constexpr (PAIR) {
@@ -274,12 +279,18 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                                 ptx::tma_load_2d(a_dst + hh * kABytes, &tmap_a, &full[stage], c0, row);
                         }
                     }
-                    if constexpr (PAIR)   // this CTA's half of the filter tile
-                        ptx::tma_load_2d_pair(b_dst, &tmap_b, full_pair, kb * BK, n0 + crank * (BN / 2));
-                    else if (!b_res)
-                        ptx::tma_load_2d(b_dst, &tmap_b, &full[stage], kb * BK, n0);
+                    // B: filter tap `tap`, input channels c0 .. c0+63 (zero past C_in), BN
+                    // output channels (zero past C_out) -- or this CTA's half of them
+                    if constexpr (PAIR) {
+                        if (!b_res)
+                            ptx::tma_load_3d_pair(b_dst, &tmap_b, full_pair, c0, tap, n0 + crank * (BN / 2));
+                        else if (first)
+                            ptx::tma_load_3d_pair(smem + p.sm.off_bres + kb * T::B_BYTES, &tmap_b, full_pair, c0,
+                                                  tap, n0 + crank * (BN / 2));
+                    } else if (!b_res)
+                        ptx::tma_load_3d(b_dst, &tmap_b, &full[stage], c0, tap, n0);
                     else if (first)
-                        ptx::tma_load_2d(smem + p.sm.off_bres + kb * T::B_BYTES, &tmap_b, &full[stage], kb * BK, n0);
+                        ptx::tma_load_3d(smem + p.sm.off_bres + kb * T::B_BYTES, &tmap_b, &full[stage], c0, tap, n0);
                     issued |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == nstages) {
@@ -301,8 +312,8 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && leader) {
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
-            constexpr uint32_t idesc_half = ptx::idesc_bf16_f32(BM, BN / 2);
-            constexpr uint32_t idesc_quarter = ptx::idesc_bf16_f32(BM, BN / 4);
+            constexpr uint32_t idesc_half = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN / 2);
+            constexpr uint32_t idesc_quarter = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN / 4);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -311,11 +322,12 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 const int kb_begin = work < p.split_from ? (work % p.splits) * p.kb_per_split : 0;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
                 // part j of a tile: N = BN/parts on rows [j*BN/parts, +BN/parts) of the resident block
-                // (MH = 1), or its 128-row half j (MH = 2)
+                // (MH = 1; with a paired MMA, rows [j*BN/parts/2, +BN/parts/2) of each CTA's half of
+                // it), or its 128-row half j (MH = 2)
                 const int part = work < p.split_from ? -1 : (work - p.split_from) % p.parts;
                 const int mh = MH > 1 && part >= 0 ? 1 : MH;
                 const uint32_t id = MH > 1 || part < 0 ? idesc : (p.parts == 2 ? idesc_half : idesc_quarter);
-                const uint32_t b_half = MH == 1 && part > 0 ? (uint32_t)(part * (BN / p.parts)) * (BK * 2) : 0u;
+                const uint32_t b_half = MH == 1 && part > 0 ? (uint32_t)(part * (BN / p.parts / CG)) * (BK * 2) : 0u;
                 const int b = T::NACC == 2 ? local & 1 : 0;
                 const uint32_t acc_phase = T::NACC == 2 ? (uint32_t)(local >> 1) & 1u : (uint32_t)local & 1u;
                 // (cluster-scope acquire for a pair: the peer's epilogue arrives here)
@@ -402,7 +414,19 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             const int mh = MH > 1 && part >= 0 ? 1 : MH;     // 128-row halves of this item
             const int width = npart ? BN / p.parts : BN;       // channels of this item
             const int m0 = ((tile / p.num_n_tiles) * CL + crank) * (BM * MH) + (MH > 1 && part > 0 ? part * BM : 0);
-            const int n0 = (tile % p.num_n_tiles) * BN + (npart && part > 0 ? part * width : 0);
+            const int tile_n0 = (tile % p.num_n_tiles) * BN;
+            const int n0 = tile_n0 + (npart && part > 0 ? part * width : 0);
+            // First output channel of accumulator columns [32c, 32c+32).  A part of
+            // a paired MMA's tile reads width/2 rows of each CTA's half of the
+            // filter block: its first width/2 columns are channels from the first
+            // half, the rest from the second.
+            auto chan = [&](int c) -> int {
+                if (PAIR && npart) {
+                    const int hw = width / 2, r0 = part * hw;
+                    return tile_n0 + (c * 32 < hw ? r0 + c * 32 : BN / 2 + r0 + (c * 32 - hw));
+                }
+                return n0 + c * 32;
+            };
             const int b = T::NACC == 2 ? local & 1 : 0;
             const uint32_t acc_phase = T::NACC == 2 ? (uint32_t)(local >> 1) & 1u : (uint32_t)local & 1u;
             const int slice_key = 8 * n0 + (npart ? p.parts : 0);   // the channels and width the slice must hold
@@ -412,8 +436,10 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 for (int i = 0; i < kChunks; ++i) {
                     const int c = h + i * (kEpiWarps / 4);
                     // chunks past the item's width (a tile part's) are not needed
-                    sv[i] = c * 32 < width ? __ldg(p.scale + n0 + c * 32 + lane) : 0.0f;
-                    bv[i] = c * 32 < width ? __ldg(p.bias + n0 + c * 32 + lane) : 0.0f;
+                    // and channels past C_out (the last channel tile's) are masked
+                    const bool in = c * 32 < width && chan(c) + lane < p.C_out;
+                    sv[i] = in ? __ldg(p.scale + chan(c) + lane) : 0.0f;
+                    bv[i] = in ? __ldg(p.bias + chan(c) + lane) : 0.0f;
                 }
                 __syncwarp();   // every lane is done with the previous tile's values
 #pragma unroll
@@ -443,7 +469,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                         ptx::tmem_ld_wait();
                         const int m = prow + lane;
                         if (m < p.M) {
-                            float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)split * p.M + m) * p.C_out + n0 + c * 32);
+                            float4 *dst = reinterpret_cast<float4 *>(p.ws + ((int64_t)split * p.M + m) * p.C_out + chan(c));
 #pragma unroll
                             for (int j = 0; j < 8; ++j)
                                 dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
@@ -477,11 +503,29 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                             *reinterpret_cast<uint4 *>(box + lane * 64 + pj * 16) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
                         }
                     }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (prow < p.M) ptx::tma_store_2d(&tmap_y, box, n0 + c * 32, prow);
-                        ptx::bulk_commit_group();
+                    const int ch0 = chan(c);
+                    if (p.y_direct) {
+                        // rows of y not 16-byte multiples: lane l copies channel ch0 + l of
+                        // each of the box's 32 rows (64 contiguous bytes per row and store)
+                        __syncwarp();
+                        const bool col_ok = ch0 + lane < p.C_out;
+                        uint16_t *y16 = reinterpret_cast<uint16_t *>(p.y);
+#pragma unroll 4
+                        for (int r = 0; r < 32; ++r) {
+                            const int pj = (lane >> 3) ^ ((r >> 1) & 3);
+                            const uint16_t v = *reinterpret_cast<const uint16_t *>(box + r * 64 + pj * 16 + (lane & 7) * 2);
+                            if (col_ok && prow + r < p.M) y16[(int64_t)(prow + r) * p.C_out + ch0 + lane] = v;
+                        }
+                        __syncwarp();   // the box is read before the next chunk overwrites it
+                    } else {
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            // the store clips at the tensor's edges (rows past M, channels
+                            // past C_out); a box wholly past either is not issued
+                            if (prow < p.M && ch0 < p.C_out) ptx::tma_store_2d(&tmap_y, box, ch0, prow);
+                            ptx::bulk_commit_group();
+                        }
                     }
                 }
             }
@@ -544,13 +588,18 @@ EncodeIm2colFn encode_im2col()
     return fn;
 }
 
+// Channel tile width: the widest of 256/128/64/32 dividing C_out; for other
+// channel counts the smallest of them covering C_out (256 beyond), so that
+// only the last tile is partial.
 int pick_bn(int C_out)
 {
     if (C_out % 256 == 0) return 256;
     if (C_out % 128 == 0) return 128;
     if (C_out % 64 == 0) return 64;
     if (C_out % 32 == 0) return 32;
-    return 0;
+    for (int bn : {32, 64, 128})
+        if (C_out <= bn) return bn;
+    return 256;
 }
 
 bool is_plain_gemm(const tf_conv_shape &s)
@@ -573,12 +622,13 @@ bool plan_smem(int num_kb, bool want_bres, SmemPlan &sm)
                            1024;   // + alignment slack
     constexpr int b_bytes = Tile<BN, MH, CG>::B_BYTES;
     const int64_t bres_bytes = (int64_t)num_kb * b_bytes;
-    sm.b_res = MH == 1 && CG == 1 && want_bres && bres_bytes <= kBResMaxBytes &&
+    sm.b_res = MH == 1 && want_bres && bres_bytes <= kBResMaxBytes &&
                (kSmemLimit - kFixed - bres_bytes) / kABytes >= 3;
     sm.stage_bytes = MH * kABytes + (sm.b_res ? 0 : b_bytes);
     const int64_t room = kSmemLimit - kFixed - (sm.b_res ? bres_bytes : 0);
     sm.stages = (int)(room / sm.stage_bytes);
-    if (sm.stages > kMaxStages) sm.stages = kMaxStages;
+    const int cap = sm.b_res ? kMaxStages : kMaxStagesStreamed;
+    if (sm.stages > cap) sm.stages = cap;
     if (sm.stages < 2) return false;
     sm.off_bres = sm.stages * sm.stage_bytes;
     sm.off_out = sm.off_bres + (sm.b_res ? (int)bres_bytes : 0);
@@ -600,6 +650,23 @@ inline void split_wide_tail(UmmaParams &p, int units)
     }
 }
 
+// The last, partial wave of tiles with a resident filter block and one
+// channel tile as quarter or half tiles over 4 or 2 times the units, when that
+// still fits in one wave; each part is at least `min_width` channels wide
+// (measured 2-2.5% off the 1x1 workload's time on single CTAs).
+inline void split_channel_tail(UmmaParams &p, int units, int bn, int min_width)
+{
+    const int rem = p.num_tiles % units;
+    for (int parts : {4, 2}) {
+        if (rem > 0 && parts * rem <= units && bn / parts >= min_width) {
+            p.split_from = p.num_tiles - rem;
+            p.parts = parts;
+            p.num_work = p.split_from + parts * rem;
+            return;
+        }
+    }
+}
+
 template <int BN, bool IM2COL, int CL, int EPI, int MH = 1, int CG = 1>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty, UmmaParams p,
                       bool want_bres, cudaStream_t st)
@@ -615,10 +682,13 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         p.split_from = p.num_work;
         p.parts = 1;
     }
-    // the channel tiles must cover C_out exactly: no filter box or parameter
-    // read past the last channel
-    if (p.num_n_tiles * BN != p.C_out) return cudaErrorNotSupported;
-    if (!plan_smem<BN, EPI, MH, CG>(p.num_kb, want_bres && CL == 1 && p.splits == 1, p.sm))
+    // the channel tiles cover C_out, and only the last one may be partial
+    // (its filter rows past C_out zero-filled, its parameters masked, its
+    // stores clipped): no filter box or store starts past the last channel
+    if (p.num_n_tiles * BN < p.C_out || (p.num_n_tiles - 1) * BN >= p.C_out) return cudaErrorNotSupported;
+    // a paired MMA's second CTA loads filter rows from BN/2 on: whole tiles only
+    if (CG == 2 && p.num_n_tiles * BN != p.C_out) return cudaErrorNotSupported;
+    if (!plan_smem<BN, EPI, MH, CG>(p.num_kb, want_bres && p.splits == 1, p.sm))
         return cudaErrorNotSupported;
     // Per-function, per-device attribute; cheap enough to set on every launch.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.sm.alloc);
@@ -640,21 +710,9 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         // channel tile c % num_n_tiles
         if (p.sm.b_res) grid = grid / p.num_n_tiles * p.num_n_tiles;
         if (grid < 1) return cudaErrorNotSupported;
-        // the last, partial wave of tiles as quarter or half tiles over 4 or 2
-        // times the CTAs, when that still fits in one wave (resident block,
-        // one channel tile; measured 2-2.5% off the 1x1 workload's time)
         if (MH > 1) split_wide_tail(p, grid);
-        if (MH == 1 && p.sm.b_res && p.num_n_tiles == 1 && p.splits == 1 && BN >= 64) {
-            const int rem = p.num_tiles % grid;
-            for (int parts : {4, 2}) {
-                if (rem > 0 && parts * rem <= grid && BN / parts >= 32) {
-                    p.split_from = p.num_tiles - rem;
-                    p.parts = parts;
-                    p.num_work = p.split_from + parts * rem;
-                    break;
-                }
-            }
-        }
+        if (MH == 1 && p.sm.b_res && p.num_n_tiles == 1 && p.C_out == BN && p.splits == 1)
+            split_channel_tail(p, grid, BN, 32);
         if (grid > p.num_work) grid = p.num_work;
         cfg.gridDim = dim3((unsigned)grid);
         cfg.numAttrs = 1;
@@ -672,8 +730,14 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         int clusters = 0;
         e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
         if (e != cudaSuccess) return e;
+        // a resident filter block pins each pair to one channel tile
+        if (p.sm.b_res) clusters = clusters / p.num_n_tiles * p.num_n_tiles;
         if (clusters < 1) return cudaErrorNotSupported;
         if (MH > 1) split_wide_tail(p, clusters);
+        // a part of a paired MMA takes half its channels from each CTA's half
+        // of the block, in whole 32-channel chunks: parts of >= 64 channels
+        if (MH == 1 && p.sm.b_res && p.num_n_tiles == 1 && p.C_out == BN && p.splits == 1)
+            split_channel_tail(p, clusters, BN, 64);
         if (clusters > p.num_work) clusters = p.num_work;
         cfg.gridDim = dim3(CL * clusters);
         return cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
@@ -714,7 +778,7 @@ cudaError_t launch_im(int bn, const CUtensorMap &ta, const CUtensorMap &tb, cons
 int choose_bn(const tf_conv_shape &s, int splits, int cl, bool pair_mma)
 {
     int bn = pick_bn(s.C_out);
-    const int num_kb = s.KH * s.KW * s.C_in / BK;
+    const int num_kb = s.KH * s.KW * ((s.C_in + BK - 1) / BK);
     const int kb_per_split = (num_kb + splits - 1) / splits;
     if (bn == 256 && short_k(kb_per_split) && !pair_mma) {
         const bool resident = cl == 1 && splits == 1 && (int64_t)num_kb * Tile<256>::B_BYTES <= kBResMaxBytes;
@@ -727,7 +791,9 @@ int choose_bn(const tf_conv_shape &s, int splits, int cl, bool pair_mma)
 
 bool conv_umma_supports(const tf_conv_shape &s, int Ho, int Wo)
 {
-    if (s.C_in % BK != 0 || pick_bn(s.C_out) == 0) return false;
+    // any C_in the API takes (a multiple of 8: 16-byte rows for TMA); the last
+    // 64-channel block of each filter tap is zero-filled past C_in
+    if (s.C_in % 8 != 0 || s.C_out < 1) return false;
     if ((int64_t)s.N * Ho * Wo >= (int64_t)1 << 31) return false;
     if (is_plain_gemm(s)) return true;
     // im2col geometry: traversal strides up to 8, filter taps addressed by
@@ -754,12 +820,17 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     // kernel is built for BN = 256), no K split
     if (a.wide && (pick_bn(s.C_out) != 256 || a.splits > 1)) return cudaErrorNotSupported;
     if (pair && a.splits > 1) return cudaErrorNotSupported;
+    // channel tails (C_out % 32 != 0) run on single CTAs without a K split
+    if (s.C_out % 32 != 0 && (pair || a.splits > 1)) return cudaErrorNotSupported;
     const int bn = a.wide ? 256 : choose_bn(s, a.splits > 1 ? a.splits : 1, cl, pair);
     const int64_t M = (int64_t)s.N * a.Ho * a.Wo;
-    const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
+    const int taps = s.KH * s.KW;
+    const int cblocks = (s.C_in + BK - 1) / BK;   // 64-channel K steps per filter tap
+    const bool y_direct = s.C_out % 8 != 0;       // y rows not 16-byte multiples: no TMA store
 
     CUtensorMap ta, tb, ty;
-    {   // y: the NHWC output as a [M][C_out] matrix, stored in 32 x 32 boxes
+    memset(&ty, 0, sizeof ty);
+    if (!y_direct) {   // y: the NHWC output as a [M][C_out] matrix, stored in 32 x 32 boxes
         const cuuint64_t dims[2] = {(cuuint64_t)s.C_out, (cuuint64_t)M};
         const cuuint64_t strides[1] = {(cuuint64_t)s.C_out * 2};
         const cuuint32_t box[2] = {kOutBox, kOutBox};
@@ -769,12 +840,14 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    {   // B: packed filters as a [C_out][K] K-major matrix (half a tile's rows per CTA of a pair)
-        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)s.C_out};
-        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {BK, (cuuint32_t)(pair ? bn / 2 : bn)};
-        const cuuint32_t estr[2] = {1, 1};
-        if (tiled(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.w), dims, strides, box, estr,
+    {   // B: packed filters [C_out][tap][C_in] (OHWI); a box is 64 input channels of one
+        // tap for BN output channels (half of them per CTA of a pair), K-major,
+        // zero-filled past C_in and past C_out
+        const cuuint64_t dims[3] = {(cuuint64_t)s.C_in, (cuuint64_t)taps, (cuuint64_t)s.C_out};
+        const cuuint64_t strides[2] = {(cuuint64_t)s.C_in * 2, (cuuint64_t)taps * s.C_in * 2};
+        const cuuint32_t box[3] = {BK, 1, (cuuint32_t)(pair ? bn / 2 : bn)};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (tiled(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.w), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
@@ -819,11 +892,12 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     p.stride_w = s.stride_w;
     p.pad_h = s.pad_h;
     p.pad_w = s.pad_w;
-    p.cblocks = s.C_in / BK;
-    p.num_kb = (int)(K / BK);
-    p.num_n_tiles = s.C_out / bn;
+    p.cblocks = cblocks;
+    p.num_kb = taps * cblocks;
+    p.num_n_tiles = (s.C_out + bn - 1) / bn;
     p.num_tiles = (int)(((M + BM - 1) / BM + cl - 1) / cl) * p.num_n_tiles;   // cl vertically adjacent tiles each
     p.epilogue = a.epilogue;
+    p.y_direct = y_direct ? 1 : 0;
     p.splits = 1;
     p.kb_per_split = p.num_kb;
     p.ws = nullptr;
@@ -838,7 +912,7 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     p.split_from = p.num_work;   // no tile parts unless launch_bn decides so
     p.parts = 1;
     if (p.err == nullptr) return cudaErrorInitializationError;
-    const bool want_bres = cl == 1 && p.splits == 1;
+    const bool want_bres = p.splits == 1;
     if (a.wide && pair)
         return im2col ? launch_bn<256, true, 2, kEpiWarpsLongK, 2, 2>(ta, tb, ty, p, false, st)
                       : launch_bn<256, false, 2, kEpiWarpsLongK, 2, 2>(ta, tb, ty, p, false, st);
@@ -846,8 +920,8 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
         return im2col ? launch_bn<256, true, 1, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st)
                       : launch_bn<256, false, 1, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st);
     if (pair)
-        return im2col ? launch_im<true, 2, 2>(bn, ta, tb, ty, p, false, st)
-                      : launch_im<false, 2, 2>(bn, ta, tb, ty, p, false, st);
+        return im2col ? launch_im<true, 2, 2>(bn, ta, tb, ty, p, want_bres, st)
+                      : launch_im<false, 2, 2>(bn, ta, tb, ty, p, want_bres, st);
     return im2col ? launch_im<true, 1>(bn, ta, tb, ty, p, want_bres, st)
                   : launch_im<false, 1>(bn, ta, tb, ty, p, want_bres, st);
 }
@@ -856,11 +930,12 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
 
 int conv_umma_splits(const tf_conv_shape &s, int Ho, int Wo)
 {
+    // whole channel tiles only: the fp32 partials are written as 128-byte rows
+    if (s.C_out % 32 != 0) return 1;
     const int bn = pick_bn(s.C_out);
-    if (bn == 0) return 1;
     const int64_t M = (int64_t)s.N * Ho * Wo;
     const int64_t tiles = (M + BM - 1) / BM * (s.C_out / bn);
-    const int64_t num_kb = (int64_t)s.KH * s.KW * s.C_in / BK;
+    const int64_t num_kb = (int64_t)s.KH * s.KW * ((s.C_in + BK - 1) / BK);
     const int sms = sm_count();
     if (tiles * 2 > sms) return 1;          // at least half the SMs busy already
     if (num_kb < 16) return 1;              // short K loops: the extra reduction costs more than it saves

@@ -174,6 +174,17 @@ __device__ __forceinline__ void tma_load_im2col_4d(void *dst, const void *map, u
         : "memory");
 }
 
+// 3-D tiled load of the box at (c0 innermost, c1, c2); completes its bytes on
+// the mbarrier.  Box elements outside the tensor are zero-filled.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *map, uint64_t *bar, int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // CTA-pair forms of the two loads above (.cta_group::2): the box lands in
 // this CTA's shared memory, and the completed bytes are counted on the
 // mbarrier at `bar_cluster`, a shared::cluster address that may lie in the
@@ -185,6 +196,16 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const void *map, uin
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(map), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const void *map, uint32_t bar_cluster, int c0, int c1,
+                                                 int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
         : "memory");
 }
 

@@ -97,17 +97,23 @@ int check_conv_shape(const tf_conv_shape *s, int *Ho, int *Wo)
 // Kernel choice by shape ("Fusing an Epilogue", "Three kernels for one
 // operation").  Thresholds measured on GB300 by
 // gemm_conv_epilogues_gb300/dispatch_sweep.py (GPU time of CUDA-graph
-// replays over 108 shapes):
-//  - the tensor-core kernel wins wherever it can run, except on tiny
-//    reductions (K = C_in*KH*KW <= 64 and under 6 MFLOP), where its fixed
-//    cost (~3.2 us for one persistent wave) ties or loses to the direct
-//    kernel;
-//  - im2col shapes with 256-channel tiles and at least a wave of 512-pixel
-//    pair tiles run wide tiles on CTA pairs with the paired MMA
-//    (tcgen05 cta_group::2: each CTA holds half of every filter tile and the
-//    two SMs' tensor cores read both halves);
-//  - other long reductions (K > 1024) over at least two waves of 128-pixel
-//    tiles run the paired MMA on 128-pixel tiles per CTA;
+// replays over 200 shapes):
+//  - the tensor-core kernel wins wherever it can run, except on tiny 1x1
+//    reductions (K = C_in*KH*KW <= 64 under 6 MFLOP, or under 12 MFLOP when
+//    C_in is not a multiple of 64), where its fixed cost (~3.2 us for one
+//    persistent wave) ties or loses to the direct kernel, and for C_in < 16:
+//    there each 64-channel K step carries 8 real channels, fetched in 16-byte
+//    pieces, so it only pays from 15 MFLOP and 48 output channels (16 for a
+//    plain 1x1, whose single K step per tile costs little);
+//  - im2col shapes with 256-channel tiles, long reductions (>= 32 K steps of
+//    64) and at least a wave of 512-pixel pair tiles run wide tiles on CTA
+//    pairs with the paired MMA (tcgen05 cta_group::2: each CTA holds half of
+//    every filter tile and the two SMs' tensor cores read both halves);
+//  - im2col shapes over at least two waves of 128-pixel tiles run the paired
+//    MMA on 128-pixel tiles per CTA when a single CTA would split the
+//    channels further (C_out % 256 == 0 with a short K loop, where it drops
+//    to 128-channel tiles) or when C_in is not a multiple of 64 (each CTA
+//    then fetches half the zero-padded filter tiles), from 64 channels;
 //  - among the CUDA-core kernels the tiled one wins from 16384 output pixels
 //    up, or with few input channels (<= 16) once there are at least ~2M
 //    output-channel-taps (M * C_out * KH * KW) to share each staged halo.
@@ -116,17 +122,22 @@ int select_variant(const tf_conv_shape &s, int Ho, int Wo)
     const int64_t M = (int64_t)s.N * Ho * Wo;
     const int64_t K = (int64_t)s.KH * s.KW * s.C_in;
     const double flops = 2.0 * (double)M * s.C_out * (double)K;
-    if (conv_umma_supports(s, Ho, Wo) && !(K <= 64 && flops < 6.0e6)) {
+    const bool cin_tail = s.C_in % 64 != 0;
+    const bool plain = s.KH == 1 && s.KW == 1 && s.stride_h == 1 && s.stride_w == 1 && s.pad_h == 0 &&
+                       s.pad_w == 0;
+    bool tc = conv_umma_supports(s, Ho, Wo);
+    if (s.C_in < 16)
+        tc = tc && flops >= 15.0e6 && s.C_out >= (plain ? 16 : 48);
+    else if (K <= 64)
+        tc = tc && flops >= (cin_tail ? 12.0e6 : 6.0e6);
+    if (tc) {
         const int64_t sms = sm_count();
-        // im2col shapes with 256-channel tiles and at least a wave of 512-pixel
-        // pair tiles: wide tiles on paired MMAs (plain 1x1 GEMMs keep their
-        // resident filter block)
-        const bool plain = s.KH == 1 && s.KW == 1 && s.stride_h == 1 && s.stride_w == 1 && s.pad_h == 0 &&
-                           s.pad_w == 0;
+        const int64_t num_kb = (int64_t)s.KH * s.KW * ((s.C_in + 63) / 64);
         const int64_t wide_tiles = (M + 511) / 512 * (s.C_out / 256);
-        if (!plain && s.C_out % 256 == 0 && wide_tiles >= sms / 2) return TF_CONV_UMMA_PAIR_WIDE;
-        // other long reductions over at least two waves of tiles: CTA pairs
-        return K > 1024 && M >= 2 * 128 * sms ? TF_CONV_UMMA_PAIR : TF_CONV_UMMA;
+        if (!plain && s.C_out % 256 == 0 && num_kb >= 32 && wide_tiles >= sms / 2) return TF_CONV_UMMA_PAIR_WIDE;
+        const bool pair_pays = cin_tail ? s.C_out >= 64 : (s.C_out % 256 == 0 && num_kb <= 16);
+        if (!plain && s.C_out % 32 == 0 && M >= 2 * 128 * sms && pair_pays) return TF_CONV_UMMA_PAIR;
+        return TF_CONV_UMMA;
     }
     const double taps = (double)M * s.C_out * s.KH * s.KW;
     if (M >= 16384 || (s.C_in <= 16 && taps >= 2.0e6)) return TF_CONV_TILED;

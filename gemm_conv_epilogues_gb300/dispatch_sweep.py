@@ -56,12 +56,15 @@ def _time_us(fn, reps: int) -> float:
 
 
 def shapes(quick: bool):
-    couts = [8, 16, 32, 64, 128, 256]
-    cins = [8, 64, 256] if not quick else [8, 64]
+    couts = [8, 16, 20, 32, 48, 64, 128, 256]
+    cins = [8, 24, 64, 256] if not quick else [8, 64]
     spatial = [(1, 16, 16), (4, 32, 32), (16, 64, 64)] if not quick else [(1, 16, 16), (4, 32, 32)]
     kernels = [(1, 0), (3, 1)]
     for co, ci, (n, h, w), (k, p) in itertools.product(couts, cins, spatial, kernels):
         yield synth.ConvShape(n, h, w, ci, co, k, k, (1, 1), (p, p))
+    if not quick:   # long reductions (up to the 7x7 workload's 25088)
+        for co, (k, p) in itertools.product([128, 256, 512], [(3, 1), (7, 3)]):
+            yield synth.ConvShape(16, 64, 64, 512, co, k, k, (1, 1), (p, p))
 
 
 def run(quick: bool = False):
@@ -98,9 +101,9 @@ def run(quick: bool = False):
 
 
 def markdown(rows) -> str:
-    out = ["| N,H,W | C_in | C_out | k | MFLOP | direct us | tiled us | umma us | pair us | wide us | umma+splitk us "
-           "| fastest | dispatch | dispatch / fastest |",
-           "|---|---:|---:|---:|---:|---:|---:|---:|---:|---:|---:|---|---|---:|"]
+    out = ["| N,H,W | C_in | C_out | k | MFLOP | direct us | tiled us | umma us | pair us | pair wide us | wide us "
+           "| umma+splitk us | fastest | dispatch | dispatch / fastest |",
+           "|---|---:|---:|---:|---:|---:|---:|---:|---:|---:|---:|---:|---|---|---:|"]
     for r in rows:
         f = lambda k: f"{r['us'][k]:.1f}" if k in r["us"] else "-"
         # the dispatch never uses a workspace: compare it with the best kernel that needs none
@@ -108,6 +111,7 @@ def markdown(rows) -> str:
         ratio = plain[r["dispatch"]] / min(plain.values()) if r["dispatch"] in plain else float("nan")
         out.append(f"| {r['N']},{r['H']},{r['W']} | {r['C_in']} | {r['C_out']} | {r['K']} | {r['mflop']:.1f} | "
                    f"{f('direct')} | {f('tiled')} | {f('umma')} | {f('umma pair')} | {f('umma pair, wide tiles')} | "
+                   f"{f('umma, wide tiles')} | "
                    f"{f('umma+splitk')} | {r['best']} | {r['dispatch']} | {ratio:.2f} |")
     agree = sum(r["best"] == r["dispatch"] for r in rows)
     out.append(f"\ndispatch picks the fastest kernel in {agree} of {len(rows)} shapes")

@@ -67,8 +67,9 @@ def test_host_validation_rejects_before_launch(native_lib):
     zero = b.conv_shape(0, 16, 16, 8, 16, 3, 3, (1, 1), (1, 1))
     assert b.tf_conv2d_bn_silu(p16, p16, p16, p16, p16, zero, 0, check=False) == S
     assert b.tf_conv2d_bn_silu_variant(p16, p16, p16, p16, p16, shape, 7, 0, check=False) == S
-    # the tensor-core kernel needs C_in % 64 == 0
-    assert b.tf_conv2d_bn_silu_variant(p16, p16, p16, p16, p16, shape, b.TF_CONV_UMMA, 0, check=False) == U
+    # the paired tensor-core kernel needs whole 32-channel tiles (C_out 16 here);
+    # rejected on the host before any launch
+    assert b.tf_conv2d_bn_silu_variant(p16, p16, p16, p16, p16, shape, b.TF_CONV_UMMA_PAIR, 0, check=False) == U
     assert b.tf_bias_gelu(p16, p16, p16, 0, 8, 0, check=False) == S
     assert b.tf_bias_gelu(p16, None, p16, 4, 8, 0, check=False) == S
     assert b.tf_bias_gelu(p16, p16, p16, 4, 12, 0, check=False) == U
@@ -126,16 +127,20 @@ def test_dispatch_selects_by_shape(native_lib):
     assert sel(w["conv3x3_tiny_1x16x16x8_to16"].conv) == b.TF_CONV_DIRECT
     assert sel(w["conv1x1_32x56x56x256_to256"].conv) == b.TF_CONV_UMMA
     assert sel(w["conv7x7_16x64x64x512_to512"].conv) == b.TF_CONV_UMMA_PAIR_WIDE   # long K, many 256-channel tiles
-    assert sel(synth.ConvShape(16, 64, 64, 512, 128, 7, 7, (1, 1), (3, 3))) == b.TF_CONV_UMMA_PAIR   # 128 channels
+    assert sel(synth.ConvShape(16, 64, 64, 512, 128, 7, 7, (1, 1), (3, 3))) == b.TF_CONV_UMMA   # 128 channels
     assert sel(synth.ConvShape(1, 64, 64, 512, 256, 7, 7, (1, 1), (3, 3))) == b.TF_CONV_UMMA   # too few tiles
-    assert sel(synth.ConvShape(16, 64, 64, 64, 256, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_UMMA_PAIR_WIDE   # short K too
+    # short K with 256 channels over two waves: paired MMA (single CTAs would take 128-channel tiles)
+    assert sel(synth.ConvShape(16, 64, 64, 64, 256, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_UMMA_PAIR
     assert sel(synth.ConvShape(16, 64, 64, 256, 256, 1, 1)) == b.TF_CONV_UMMA   # plain 1x1: resident filters
     assert sel(synth.ConvShape(1, 16, 16, 64, 256, 1, 1)) == b.TF_CONV_UMMA   # 8.4 MFLOP: tensor cores win
-    # shapes the tensor-core kernel cannot take go to the CUDA-core kernels
-    assert sel(synth.ConvShape(16, 32, 32, 24, 48, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
-    assert sel(synth.ConvShape(4, 32, 32, 8, 64, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
+    # channel tails run on the tensor cores too (C_in >= 16 or enough work)
+    assert sel(synth.ConvShape(16, 32, 32, 24, 48, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_UMMA
+    assert sel(synth.ConvShape(4, 32, 32, 256, 16, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_UMMA
+    assert sel(synth.ConvShape(16, 64, 64, 24, 128, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_UMMA_PAIR   # C_in tail
+    assert sel(synth.ConvShape(4, 32, 32, 8, 64, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_UMMA
+    # few input channels and few outputs stay on the CUDA cores
     assert sel(synth.ConvShape(4, 32, 32, 8, 32, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_DIRECT
-    assert sel(synth.ConvShape(4, 32, 32, 256, 16, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_DIRECT
+    assert sel(synth.ConvShape(16, 64, 64, 8, 32, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
     # tiny reductions stay on the direct kernel even when the tensor-core one could run
     assert sel(synth.ConvShape(1, 16, 16, 64, 64, 1, 1)) == b.TF_CONV_DIRECT
     assert sel(synth.ConvShape(1, 16, 16, 256, 64, 1, 1)) == b.TF_CONV_UMMA

@@ -132,6 +132,61 @@ def test_conv_umma_small(b, c, variant):
     _assert_no_device_error(b)
 
 
+# Channel tails on the tensor-core kernel: C_in not a multiple of 64 (the last
+# 64-channel block of each tap zero-filled by TMA, in the filters through
+# their 3-D tensor map) and C_out not a multiple of 32 (the last channel
+# tile's filter rows zero-filled, its scale/bias masked, its stores clipped;
+# C_out % 8 != 0 stores rows that TMA cannot address with masked plain
+# stores).  Every output against the oracle.
+TAIL_SHAPES = [
+    synth.ConvShape(4, 32, 32, 256, 16, 3, 3, (1, 1), (1, 1)),      # C_out 16: one half-empty 32-channel tile
+    synth.ConvShape(2, 17, 19, 64, 20, 3, 3, (1, 1), (1, 1)),       # C_out 20: direct stores, ragged M
+    synth.ConvShape(2, 20, 20, 128, 48, 3, 3, (2, 2), (1, 1)),      # C_out 48 in a 64 tile, stride 2
+    synth.ConvShape(1, 23, 21, 64, 200, 1, 1, (1, 1), (0, 0)),      # C_out 200 in a 256 tile, resident filters
+    synth.ConvShape(2, 16, 16, 8, 32, 3, 3, (1, 1), (1, 1)),        # C_in 8: 8 of 64 channels per K step
+    synth.ConvShape(1, 18, 18, 24, 64, 5, 5, (1, 1), (2, 2)),       # C_in 24
+    synth.ConvShape(3, 11, 13, 40, 96, 1, 1, (1, 1), (0, 0)),       # C_in 40, plain GEMM, 3 tiles of 32
+    synth.ConvShape(1, 16, 16, 8, 16, 3, 3, (1, 1), (1, 1)),        # both tails, tiny
+    synth.ConvShape(2, 14, 14, 40, 20, 7, 7, (1, 1), (3, 3)),       # both tails, 7x7, direct stores
+    synth.ConvShape(1, 20, 20, 72, 300, 3, 3, (1, 1), (1, 1)),      # C_in 64 + 8; C_out 300 = 256 + 44
+    synth.ConvShape(2, 9, 9, 136, 5, 1, 1, (1, 1), (0, 0)),         # odd C_out 5: 2-byte rows
+]
+
+
+@pytest.mark.parametrize("c", TAIL_SHAPES, ids=lambda c: f"{c.N}x{c.H}x{c.W}x{c.C_in}-{c.C_out}k{c.KH}s{c.stride[0]}")
+def test_conv_umma_channel_tails(b, c):
+    d = synth.conv_inputs(c, seed=18, w_dist="normal_fanin")
+    got = _run_conv(b, c, d, b.TF_CONV_UMMA)
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    _conv_check(got, ref)
+    _assert_no_device_error(b)
+
+
+# C_in tails on the paired and wide-tile kernels (which need whole channel tiles)
+@pytest.mark.parametrize("variant,c", [
+    (3, synth.ConvShape(2, 16, 16, 24, 64, 3, 3, (1, 1), (1, 1))),
+    (3, synth.ConvShape(1, 30, 30, 40, 256, 1, 1, (1, 1), (0, 0))),    # paired MMA, resident halves, tail parts
+    (4, synth.ConvShape(2, 20, 20, 40, 256, 3, 3, (1, 1), (1, 1))),
+    (5, synth.ConvShape(1, 24, 24, 72, 256, 3, 3, (1, 1), (1, 1))),
+], ids=["pair-cin24", "pair-1x1-cin40", "pairwide-cin40", "wide-cin72"])
+def test_conv_umma_input_channel_tails_other_kernels(b, variant, c):
+    d = synth.conv_inputs(c, seed=19, w_dist="normal_fanin")
+    got = _run_conv(b, c, d, variant)
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    _conv_check(got, ref)
+    _assert_no_device_error(b)
+
+
+def test_conv_umma_pair_rejects_channel_tails(b):
+    c = synth.ConvShape(1, 12, 12, 64, 48, 3, 3, (1, 1), (1, 1))
+    x = torch.zeros((c.N, c.H, c.W, c.C_in), dtype=torch.int16, device="cuda")
+    w = torch.zeros((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device="cuda")
+    sc = torch.ones((c.C_out,), dtype=torch.float32, device="cuda")
+    y = torch.zeros((c.M, c.C_out), dtype=torch.int16, device="cuda")
+    rc = b.tf_conv2d_bn_silu_variant(x, w, sc, sc, y, _shape(b, c), b.TF_CONV_UMMA_PAIR, check=False)
+    assert rc == b.TF_ERR_UNSUPPORTED
+
+
 # 256-pixel tiles per CTA on CTA pairs (C_out % 256 == 0).  With fewer tiles
 # than pairs every tile runs as its two 128-row halves (the tail split); the
 # second CTA's halves of a pair can lie past M.
@@ -183,6 +238,7 @@ SPLITK_SHAPES = [
     synth.ConvShape(1, 8, 8, 512, 128, 3, 3, (1, 1), (1, 1)),       # one ragged tile
     synth.ConvShape(2, 14, 14, 128, 64, 7, 7, (1, 1), (3, 3)),      # 7x7, ragged M tail
     synth.ConvShape(1, 12, 12, 1024, 512, 1, 1, (1, 1), (0, 0)),    # 1x1, 2 N tiles, 16 K blocks
+    synth.ConvShape(1, 10, 10, 200, 128, 3, 3, (1, 1), (1, 1)),     # C_in 200 = 3 x 64 + 8: 36 K blocks
 ]
 
 

@@ -50,11 +50,13 @@ def test_conv_random_shape_every_kernel(b, c):
     b.tf_pack_filter_nhwc(dev_u16(d["w_oihw"]), w, c.C_out, c.C_in, c.KH, c.KW)
     sc, bi = dev_f32(d["scale"]), dev_f32(d["bias"])
     shape = b.conv_shape(c.N, c.H, c.W, c.C_in, c.C_out, c.KH, c.KW, c.stride, c.pad)
-    variants = [b.TF_CONV_AUTO, b.TF_CONV_DIRECT, b.TF_CONV_TILED]
-    if c.C_in % 64 == 0 and c.C_out % 32 == 0:
-        variants += [b.TF_CONV_UMMA, b.TF_CONV_UMMA_PAIR]
-        if c.C_out % 256 == 0:
-            variants += [b.TF_CONV_UMMA_PAIR_WIDE, b.TF_CONV_UMMA_WIDE]
+    # the tensor-core kernel takes every shape here (channel tails included);
+    # its paired and wide forms need whole 32- and 256-channel tiles
+    variants = [b.TF_CONV_AUTO, b.TF_CONV_DIRECT, b.TF_CONV_TILED, b.TF_CONV_UMMA]
+    if c.C_out % 32 == 0:
+        variants.append(b.TF_CONV_UMMA_PAIR)
+    if c.C_out % 256 == 0:
+        variants += [b.TF_CONV_UMMA_PAIR_WIDE, b.TF_CONV_UMMA_WIDE]
     for v in variants:
         y = torch.full((c.M, c.C_out), 0x7FC0, dtype=torch.int16, device="cuda")   # NaN sentinel
         b.tf_conv2d_bn_silu_variant(x, w, sc, bi, y, shape, v)
