@@ -20,6 +20,7 @@ TF_OK, TF_ERR_INVALID_ARG, TF_ERR_UNSUPPORTED, TF_ERR_CUDA, TF_ERR_TIMEOUT = 0, 
 TF_LN_AUTO, TF_LN_WARP, TF_LN_CTA, TF_LN_CLUSTER = -1, 0, 1, 2
 TF_DEVERR_PRODUCER_WAIT, TF_DEVERR_MMA_WAIT, TF_DEVERR_EPILOGUE_WAIT = 0x1, 0x2, 0x4
 TF_DEVERR_DRAIN_WAIT, TF_DEVERR_PROBE_WAIT, TF_DEVERR_EXCHANGE_WAIT = 0x8, 0x10, 0x20
+TF_DEVERR_PAIR_TMEM, TF_DEVERR_SMEM_ALIGN = 0x40, 0x80
 
 
 class TfError(RuntimeError):

@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(TH * TW) conv_tiled_kernel(ConvArgs a, int hal
     for (int j = 0; j < CO_T; ++j) acc[j] = 0.0f;
 
     for (int c0 = 0; c0 < s.C_in; c0 += CI_T) {
-        __syncthreads();
+        cta_sync();
         for (int i = threadIdx.x; i < halo_h * halo_w; i += blockDim.x) {
             const int ih = ih0 + i / halo_w, iw = iw0 + i % halo_w;
             uint4 v = zero;
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(TH * TW) conv_tiled_kernel(ConvArgs a, int hal
             if (co < s.C_out) v = __ldg(reinterpret_cast<const uint4 *>(w + ((int64_t)co * taps + t) * s.C_in + c0));
             ws[i] = v;
         }
-        __syncthreads();
+        cta_sync();
         for (int kh = 0; kh < s.KH; ++kh) {
             for (int kw = 0; kw < s.KW; ++kw) {
                 float xf[8];

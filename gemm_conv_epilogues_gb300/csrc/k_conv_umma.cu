@@ -74,7 +74,9 @@ struct Tile {
 //   [0, off_bres)          operand ring: `stages` x (A tile, + B tile unless resident)
 //   [off_bres, off_out)    resident filter block: num_kb B tiles (b_res only)
 //   [off_out, off_par)     one 2 KB output staging box per epilogue warp
-//   [off_par, off_bar)     per epilogue warp, the scale/bias values of its chunks
+//   [off_par, off_bar)     per epilogue warp, the scale/bias values of its chunks;
+//                          with a resident filter block (whose channel tile never
+//                          changes) one table of the tile's BN scales and biases
 //   [off_bar, total)       mbarriers and the TMEM address slot
 struct SmemPlan {
     int stages, stage_bytes, b_res, off_bres, off_out, off_par, off_bar, alloc;
@@ -147,8 +149,10 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     static_assert(CG == 1 || CL == 2, "a paired MMA runs on a 2-CTA cluster");
     constexpr bool PAIR = CG == 2;
     using T = Tile<BN, MH, CG>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // operand tiles use the 128-byte swizzle, whose 8-row atoms must start on
+    // 1024-byte boundaries (checked below)
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.sm.off_bar);
     uint64_t *empty = full + kMaxStages;
     uint64_t *tfull = empty + kMaxStages;
@@ -190,25 +194,29 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         }
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    cta_sync();
     ptx::tc_fence_after();
     // a pair's barriers exist in both CTAs before any copy, commit or arrival
     // from the other CTA reaches them
     if constexpr (PAIR) ptx::cluster_sync();
-    // The set-up above touched no global memory; from here on the kernel
-    // reads and writes it, so it waits for the stream's previous kernel
-    // (programmatic dependent launch), and lets the next one start its own
-    // set-up on SMs this grid leaves.
-    ptx::griddep_wait();
+    // Programmatic dependent launch: the next kernel of the stream may start
+    // its own set-up on SMs this grid leaves.  Each role waits for the
+    // stream's previous kernel (griddep_wait) only right before its first
+    // global-memory access, so that the set-up above and the first work
+    // item's address arithmetic overlap that kernel's tail.
     ptx::griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
     int num_work = p.num_work;
+    if ((ptx::smem_u32(smem) & 1023u) != 0) {   // no work on misaligned operand tiles
+        num_work = 0;
+        if (threadIdx.x == 0) atomicOr(p.err, TF_DEVERR_SMEM_ALIGN);
+    }
     if constexpr (PAIR) {
         // the paired MMA writes both CTAs' accumulators at the first CTA's
         // TMEM address: if the two allocations differ, no work is done
         if (ptx::ld_shared_cluster_u32(ptx::mapa_shared(tmem_slot, (uint32_t)crank ^ 1u)) != tmem_base) {
             num_work = 0;
-            if (threadIdx.x == 0) atomicOr(p.err, TF_DEVERR_PAIR_TMEM);
+            if (threadIdx.x == 0) atomicOr(p.err, TF_DEVERR_PAIR_TMEM);   // an OR: order-free
         }
     }
 
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, last_phase = 0;  // per-stage bit masks
-            bool ok = true;
+            bool ok = true, waited = false;
             for (int work = cid; ok && work < num_work; work += ncl) {
                 // a resident filter block streams in with the CTA's first tile:
                 // K step kb's B tile lands in its resident slot on the same
@@ -246,6 +254,10 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
                         ok = false;
                         break;
+                    }
+                    if (!waited) {   // the first copy reads memory the previous kernel may write
+                        ptx::griddep_wait();
+                        waited = true;
                     }
                     // bytes this CTA loads for the stage; with a paired MMA both CTAs
                     // load as much, and all of it completes on the first CTA's barrier
@@ -311,6 +323,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && leader) {
+            ptx::griddep_wait();   // (its only global access is the error word)
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
             constexpr uint32_t idesc_half = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN / 2);
             constexpr uint32_t idesc_quarter = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN / 4);
@@ -398,11 +411,25 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
         // in a shared-memory slice (one coalesced load per lane and chunk,
         // repeated only when the tile's channel range changes) and reads them
         // with broadcast loads.
+        ptx::griddep_wait();   // before the parameter and output accesses
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         uint8_t *box = smem + p.sm.off_out + (warp - 2) * kOutBoxBytes;
         constexpr int kChunks = chunks_per_warp(BN, kEpiWarps);
         float *slice = reinterpret_cast<float *>(smem + p.sm.off_par + (warp - 2) * kChunks * kParamChunkBytes);
+        // A resident filter block pins the CTA to one channel tile: its BN
+        // scales and biases are loaded once into a table all epilogue warps read.
+        float *table = reinterpret_cast<float *>(smem + p.sm.off_par);
+        const int cta_n0 = (cid % p.num_n_tiles) * BN;
+        if (b_res && p.epilogue == 1) {
+            for (int i = threadIdx.x - 64; i < BN; i += kEpiWarps * 32) {
+                const bool in = cta_n0 + i < p.C_out;
+                table[i] = in ? __ldg(p.scale + cta_n0 + i) : 0.0f;
+                table[BN + i] = in ? __ldg(p.bias + cta_n0 + i) : 0.0f;
+            }
+            __syncwarp();
+            asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");   // the epilogue warps only
+        }
         int slice_n0 = -1;   // 8 * first channel + parts of the item whose parameters the slice holds
         int local = 0;
         bool ok = true;
@@ -430,7 +457,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             const int b = T::NACC == 2 ? local & 1 : 0;
             const uint32_t acc_phase = T::NACC == 2 ? (uint32_t)(local >> 1) & 1u : (uint32_t)local & 1u;
             const int slice_key = 8 * n0 + (npart ? p.parts : 0);   // the channels and width the slice must hold
-            if (p.epilogue == 1 && slice_key != slice_n0) {   // before the accumulator wait, which hides the latency
+            if (!b_res && p.epilogue == 1 && slice_key != slice_n0) {   // before the accumulator wait, which hides the latency
                 float sv[kChunks], bv[kChunks];
 #pragma unroll
                 for (int i = 0; i < kChunks; ++i) {
@@ -481,8 +508,10 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                     if (lane == 0) ptx::bulk_wait_group_read<0>();
                     __syncwarp();
                     ptx::tmem_ld_wait();
-                    const float4 *s4 = reinterpret_cast<const float4 *>(slice + ci * 64);
-                    const float4 *b4 = reinterpret_cast<const float4 *>(slice + ci * 64 + 32);
+                    const int ch0 = chan(c);
+                    const float4 *s4 = reinterpret_cast<const float4 *>(b_res ? table + (ch0 - cta_n0) : slice + ci * 64);
+                    const float4 *b4 =
+                        reinterpret_cast<const float4 *>(b_res ? table + BN + (ch0 - cta_n0) : slice + ci * 64 + 32);
                     uint32_t wq[4];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -503,7 +532,6 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                             *reinterpret_cast<uint4 *>(box + lane * 64 + pj * 16) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
                         }
                     }
-                    const int ch0 = chan(c);
                     if (p.y_direct) {
                         // rows of y not 16-byte multiples: lane l copies channel ch0 + l of
                         // each of the box's 32 rows (64 contiguous bytes per row and store)
@@ -542,7 +570,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    cta_sync();
     // neither CTA of a pair frees its TMEM or exits while the pair's MMAs,
     // commits, copies or arrivals may still reach it
     if constexpr (PAIR) ptx::cluster_sync();
@@ -618,23 +646,25 @@ int upper_corner(int in, int out, int stride, int pad) { return (out - 1) * stri
 template <int BN, int EPI, int MH = 1, int CG = 1>
 bool plan_smem(int num_kb, bool want_bres, SmemPlan &sm)
 {
-    constexpr int kFixed = EPI * (kOutBoxBytes + chunks_per_warp(BN, EPI) * kParamChunkBytes) + kBarBytes +
-                           1024;   // + alignment slack
+    constexpr int kBoxes = EPI * kOutBoxBytes;
+    constexpr int kSlices = EPI * chunks_per_warp(BN, EPI) * kParamChunkBytes;   // per-warp parameter slices
+    constexpr int kTable = 2 * BN * 4;                                              // or one table (resident block)
     constexpr int b_bytes = Tile<BN, MH, CG>::B_BYTES;
     const int64_t bres_bytes = (int64_t)num_kb * b_bytes;
     sm.b_res = MH == 1 && want_bres && bres_bytes <= kBResMaxBytes &&
-               (kSmemLimit - kFixed - bres_bytes) / kABytes >= 3;
+               (kSmemLimit - (kBoxes + kTable + kBarBytes) - bres_bytes) / kABytes >= 3;
+    const int fixed = kBoxes + (sm.b_res ? kTable : kSlices) + kBarBytes;
     sm.stage_bytes = MH * kABytes + (sm.b_res ? 0 : b_bytes);
-    const int64_t room = kSmemLimit - kFixed - (sm.b_res ? bres_bytes : 0);
+    const int64_t room = kSmemLimit - fixed - (sm.b_res ? bres_bytes : 0);
     sm.stages = (int)(room / sm.stage_bytes);
     const int cap = sm.b_res ? kMaxStages : kMaxStagesStreamed;
     if (sm.stages > cap) sm.stages = cap;
     if (sm.stages < 2) return false;
     sm.off_bres = sm.stages * sm.stage_bytes;
     sm.off_out = sm.off_bres + (sm.b_res ? (int)bres_bytes : 0);
-    sm.off_par = sm.off_out + EPI * kOutBoxBytes;
-    sm.off_bar = sm.off_par + EPI * chunks_per_warp(BN, EPI) * kParamChunkBytes;
-    sm.alloc = sm.off_bar + kBarBytes + 1024;
+    sm.off_par = sm.off_out + kBoxes;
+    sm.off_bar = sm.off_par + (sm.b_res ? kTable : kSlices);
+    sm.alloc = sm.off_bar + kBarBytes;
     return sm.alloc <= kSmemLimit;
 }
 
@@ -1007,7 +1037,7 @@ __global__ void wait_probe_kernel(uint32_t *err, uint64_t limit_ns)
         ptx::mbar_init(&bar, 1);
         ptx::mbar_init_fence();
     }
-    __syncthreads();
+    cta_sync();
     // Nothing ever arrives on `bar`: phase 0 never completes, the wait gives up.
     if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0, limit_ns)) atomicOr(err, TF_DEVERR_PROBE_WAIT);
 }

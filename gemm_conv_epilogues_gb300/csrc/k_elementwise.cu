@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kRingBlock, 2) bias_gelu_ring_kernel(const uin
         }
         ptx::mbar_init_fence();
     }
-    __syncthreads();
+    cta_sync();
     if (warp == kRingThreads / 32) {
         // the copy warp: loads into free stages, stores computed ones
         if (lane != 0) return;

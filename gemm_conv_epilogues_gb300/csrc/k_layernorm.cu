@@ -39,9 +39,9 @@ __device__ __forceinline__ float block_sum(float v, float *red)
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = (blockDim.x + 31) >> 5;
-    __syncthreads();  // `red` may still be read by the previous reduction
+    cta_sync();  // `red` may still be read by the previous reduction
     if (lane == 0) red[warp] = v;
-    __syncthreads();
+    cta_sync();
     float t = lane < nwarps ? red[lane] : 0.0f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(1024) layernorm_kernel(const __half *__restric
             if (RESIDUAL) ptx::bulk_load(dst + row_bytes, b + row * hidden, row_bytes, &full[st]);
         }
     }
-    __syncthreads();
+    cta_sync();
 
     // gamma and beta stay in registers for every row this CTA handles
     float g[NV][8], bb[NV][8];
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(1024) layernorm_kernel(const __half *__restric
         const int st = it % stages;
         const uint32_t parity = (uint32_t)(it / stages) & 1u;
         const bool ok = ptx::mbar_wait(&full[st], parity, wait_ns);
-        if (!__syncthreads_and(ok)) {
+        if (!cta_sync_and(ok)) {
             if (threadIdx.x == 0) atomicOr(err, TF_DEVERR_PRODUCER_WAIT);
             break;
         }
@@ -310,9 +310,9 @@ __device__ __forceinline__ float cta_sum(float v, float *red)
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = (blockDim.x + 31) >> 5;
-    __syncthreads();
+    cta_sync();
     if (lane == 0) red[warp] = v;
-    __syncthreads();
+    cta_sync();
     float t = lane < nwarps ? red[lane] : 0.0f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
         const int pb = it & 1;
         const uint32_t xpar = (uint32_t)(it >> 1) & 1u;
         const bool ok = !failed && ptx::mbar_wait(&full[st], (uint32_t)(it / stages) & 1u, wait_ns);
-        if (!__syncthreads_and(ok) && !failed) {
+        if (!cta_sync_and(ok) && !failed) {
             failed = true;
             fail_it = it;
             if (threadIdx.x == 0) atomicOr(err, TF_DEVERR_PRODUCER_WAIT);

@@ -104,12 +104,12 @@ __global__ void __launch_bounds__(kThreads, FUSED && R >= 4 ? 3 : 4) rowsum_kern
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], o);
         }
-        __syncthreads();   // `red` of the previous tile has been read
+        cta_sync();   // `red` of the previous tile has been read
         if (lane == 0) {
 #pragma unroll
             for (int r = 0; r < R; ++r) red[warp][r] = sum[r];
         }
-        __syncthreads();
+        cta_sync();
         if (threadIdx.x < R && r0 + threadIdx.x < rows) {
             float t = 0.0f;
 #pragma unroll

@@ -157,8 +157,11 @@ __device__ __forceinline__ void griddep_launch_dependents()
 }
 
 // Barrier over all threads of all CTAs of the cluster (release/acquire).
+// The barrier is warp-aligned, so each warp is reconverged first (lanes that
+// took another path would otherwise arrive for the whole warp).
 __device__ __forceinline__ void cluster_sync()
 {
+    __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 

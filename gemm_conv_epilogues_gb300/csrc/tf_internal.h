@@ -92,6 +92,24 @@ __device__ __forceinline__ void pdl_begin()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// CTA-wide barriers for code in which the lanes of a warp may have taken
+// different paths (a role run by lane 0 alone, a divergent loop exit).  The
+// barrier instruction is warp-aligned: it counts a whole warp as arrived as
+// soon as any of its lanes arrives, so lanes that get there early would let
+// it complete before the rest of the CTA (and count the warp again later).
+// Each warp is reconverged first.  Every lane of the CTA must still be live.
+__device__ __forceinline__ void cta_sync()
+{
+    __syncwarp();
+    __syncthreads();
+}
+
+__device__ __forceinline__ int cta_sync_and(int pred)
+{
+    __syncwarp();
+    return __syncthreads_and(pred);
+}
+
 // kern<<<grid, block, smem, st>>>(args...) with programmatic dependent launch allowed.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args)

@@ -296,6 +296,8 @@ uint64_t tf_get_wait_limit_ns(void);
 #define TF_DEVERR_EXCHANGE_WAIT 0x20u /* cluster LayerNorm: a peer CTA's partial sum never arrived */
 #define TF_DEVERR_PAIR_TMEM 0x40u     /* paired conv MMA: the two CTAs' TMEM allocations differ
                                          (the pair did no work) */
+#define TF_DEVERR_SMEM_ALIGN 0x80u    /* tensor-core conv: dynamic shared memory not 1024-byte
+                                         aligned (the CTA did no work) */
 
 /* Synchronises the current device, copies the device error word of the
  * current device into *word (may be NULL), clears it, and returns TF_OK if it
