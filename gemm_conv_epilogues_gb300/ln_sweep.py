@@ -5,7 +5,11 @@ the data behind the explicit width boundaries of tf_residual_layernorm
 large enough to require a different row-reduction strategy; the dispatch
 boundary should be explicit rather than inherited from one benchmark shape).
 
-    python -m gemm_conv_epilogues_gb300.ln_sweep [--json out.json]
+    python -m gemm_conv_epilogues_gb300.ln_sweep [--json out.json] [--widths 24576,32768]
+    python -m gemm_conv_epilogues_gb300.ln_sweep --widths 32768 --variant cluster --plain 3
+
+--plain N skips the timing and just launches the chosen strategy N times on
+the width's inputs, one call after another (for profiler captures).
 
 For each width the row count is chosen so act + res + y move about 400 MB
 (more than three times the L2); each strategy is timed by CUDA-graph replay.
@@ -46,9 +50,9 @@ def _time_us(fn, reps: int = 10) -> float:
     return statistics.median(out)
 
 
-def run():
+def run(widths=WIDTHS):
     rows_out = []
-    for h in WIDTHS:
+    for h in widths:
         rows = max(1, (400 * 2**20) // (6 * h))
         d = synth.layernorm_inputs(rows, h, seed=0)
         up = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).cuda()
@@ -81,11 +85,36 @@ def markdown(rows) -> str:
     return "\n".join(out)
 
 
+def plain(h: int, variant: int, calls: int):
+    rows = max(1, (400 * 2**20) // (6 * h))
+    d = synth.layernorm_inputs(rows, h, seed=0)
+    up = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).cuda()
+    act, res = up(d["act"], np.float16), up(d["res"], np.float16)
+    g, be = up(d["gamma"], np.float32), up(d["beta"], np.float32)
+    y = torch.empty_like(act)
+    for _ in range(calls):
+        b.tf_residual_layernorm_variant(act, res, g, be, y, rows, h, 1e-5, variant)
+    torch.cuda.synchronize()
+    rc, word = b.tf_read_device_error()
+    if rc != b.TF_OK:
+        raise SystemExit(f"device error word {word:#x}")
+    print(json.dumps({"hidden": h, "rows": rows, "variant": variant, "calls": calls}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--json", default=None)
+    ap.add_argument("--widths", default=None, help="comma-separated hidden widths (default: the full list)")
+    ap.add_argument("--variant", default="auto", choices=["auto", "warp", "cta", "cluster"])
+    ap.add_argument("--plain", type=int, default=0, help="only launch the variant this many times (profiling)")
     args = ap.parse_args()
-    rows = run()
+    widths = [int(w) for w in args.widths.split(",")] if args.widths else WIDTHS
+    if args.plain:
+        v = {"auto": b.TF_LN_AUTO, "warp": b.TF_LN_WARP, "cta": b.TF_LN_CTA, "cluster": b.TF_LN_CLUSTER}[args.variant]
+        for h in widths:
+            plain(h, v, args.plain)
+        return
+    rows = run(widths)
     if args.json:
         with open(args.json, "w") as f:
             json.dump(rows, f, indent=1)

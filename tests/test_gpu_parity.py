@@ -119,6 +119,8 @@ UMMA_SHAPES = [
     synth.ConvShape(4, 41, 41, 64, 96, 3, 3, (1, 1), (1, 1)),       # 3 channel tiles of 32, several tiles per CTA
     synth.ConvShape(1, 12, 12, 64, 256, 3, 3, (1, 1), (1, 1)),      # short K, block too big: 128-wide tiles, streamed
     synth.ConvShape(1, 15, 20, 64, 64, 1, 1, (1, 1), (0, 0)),       # plain GEMM, 3 tiles: a pair's second tile wholly past M
+    # resident block, one channel tile, more tiles than CTAs: dynamic schedule, half-tile tail
+    synth.ConvShape(8, 56, 56, 64, 256, 1, 1, (1, 1), (0, 0)),
 ]
 
 
