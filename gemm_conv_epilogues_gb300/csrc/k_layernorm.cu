@@ -48,6 +48,23 @@ __device__ __forceinline__ float block_sum(float v, float *red)
     return t;
 }
 
+// The same sum with ONE barrier: shuffles within each warp, one shared-memory
+// step.  `red` must be a buffer no thread can still be reading:
+// callers alternate two, with a CTA barrier between uses of the same one.
+__device__ __forceinline__ float cta_sum_alt(float v, float *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    if (lane == 0) red[warp] = v;
+    cta_sync();
+    float t = lane < nwarps ? red[lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
+
 // Persistent CTAs walk the rows blockIdx.x, blockIdx.x + gridDim.x, ...
 // Thread 0 streams the input rows into a `stages`-deep shared-memory ring with
 // 1-D bulk copies (cp.async.bulk, completion on an mbarrier), so several rows
@@ -304,20 +321,6 @@ __device__ __forceinline__ uint32_t cluster_nctarank()
     return r;
 }
 
-__device__ __forceinline__ float cta_sum(float v, float *red)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nwarps = (blockDim.x + 31) >> 5;
-    cta_sync();
-    if (lane == 0) red[warp] = v;
-    cta_sync();
-    float t = lane < nwarps ? red[lane] : 0.0f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    return t;
-}
 
 // Wide rows (hidden > 16384): a thread-block cluster owns a row; CTA r of the
 // cluster owns the slice [r*slice, (r+1)*slice).  Clusters are persistent and
@@ -354,7 +357,8 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
     pdl_begin();
     constexpr int kMaxRanks = 16;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[32];
+    __shared__ float red[2][32];   // the row's two reductions alternate buffers
+    __shared__ int copy_fail;      // set by any thread whose wait for a stage ran out
     __shared__ __align__(8) float2 slot[2][kMaxRanks];   // [row parity][sending rank]: (sum, M2) of its slice
     __shared__ __align__(8) uint64_t xbar[2];
     const uint32_t rank = ptx::cluster_ctarank(), nranks = cluster_nctarank();
@@ -373,6 +377,7 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
         if (RESIDUAL) ptx::bulk_load(dst + (size_t)slice * 2, b + row * hidden + c0, part_bytes, &full[st]);
     };
     if (threadIdx.x == 0) {
+        copy_fail = 0;
         for (int st = 0; st < stages; ++st) ptx::mbar_init(&full[st], 1);
         for (int p = 0; p < 2; ++p) ptx::mbar_init(&xbar[p], 1);
         ptx::mbar_init_fence();
@@ -428,12 +433,10 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
         const int st = it % stages;
         const int pb = it & 1;
         const uint32_t xpar = (uint32_t)(it >> 1) & 1u;
-        const bool ok = !failed && ptx::mbar_wait(&full[st], (uint32_t)(it / stages) & 1u, wait_ns);
-        if (!cta_sync_and(ok) && !failed) {
-            failed = true;
-            fail_it = it;
-            if (threadIdx.x == 0) atomicOr(err, TF_DEVERR_PRODUCER_WAIT);
-        }
+        // a wait that runs out is reported through copy_fail, which every
+        // thread reads after the row's first reduction barrier (the values read
+        // from a stage that never filled are garbage, and the results void)
+        if (!failed && !ptx::mbar_wait(&full[st], (uint32_t)(it / stages) & 1u, wait_ns)) copy_fail = 1;
         const unsigned char *src = smem + (size_t)st * stage_bytes;
         float sv[NV][8];
         float sum = 0.0f;
@@ -460,14 +463,14 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
                 sum += f.x + f.y;
             }
         }
-        const float total = cta_sum(sum, red);   // its barriers also mean every thread has read stage `st`
-        if (threadIdx.x == 0) {
-            const int64_t next = row + (int64_t)stages * ncl;
-            if (next < rows && !failed) {
-                ptx::fence_proxy_async_smem();
-                issue(st, next);
-                issued_until = it + stages + 1;
-            }
+        // Two reductions per row, one barrier each: the sum uses red[0], the
+        // squared deviations red[1], and between a reduction and the next use
+        // of its buffer lies the other one's barrier.
+        const float total = cta_sum_alt(sum, red[0]);
+        if (copy_fail && !failed) {
+            failed = true;
+            fail_it = it;
+            if (threadIdx.x == 0) atomicOr(err, TF_DEVERR_PRODUCER_WAIT);
         }
         // this slice's own mean and sum of squared deviations from it ...
         const float mean_c = total / (float)width;
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
                 }
             }
         }
-        exchange(total, cta_sum(sq, red), pb, xpar);
+        exchange(total, cta_sum_alt(sq, red[1]), pb, xpar);
         // ... merged over the slices (Chan et al.'s pairwise update):
         // M2 = sum_r M2_r + sum_r n_r (mean_r - mean)^2, in rank order
         float tsum = 0.0f;
@@ -512,8 +515,19 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
             }
             st_stream(yr + 8 * v, out);
         }
+        // stage `st` (read by every thread before the first reduction) takes the
+        // row `stages` ahead; issued at the end of the row, off the path between
+        // the row's two reductions
+        if (threadIdx.x == blockDim.x - 1) {
+            const int64_t next = row + (int64_t)stages * ncl;
+            if (next < rows && !failed) {
+                ptx::fence_proxy_async_smem();
+                issue(st, next);
+                issued_until = it + stages + 1;
+            }
+        }
     }
-    if (threadIdx.x == 0 && failed) {   // copies issued but never consumed land before exit
+    if (threadIdx.x == blockDim.x - 1 && failed) {   // copies issued but never consumed land before exit
         for (int k = fail_it; k < issued_until; ++k) {
             const int64_t row = cid + (int64_t)k * ncl;
             if (row >= rows) break;
