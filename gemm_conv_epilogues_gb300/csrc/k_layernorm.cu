@@ -423,6 +423,12 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
     };
 
     const float inv_h = 1.0f / (float)hidden;
+    const float inv_w = 1.0f / (float)width;
+    // Merge terms of rank r (lane r of every warp): its column count and its
+    // reciprocal, fixed for the kernel
+    const uint32_t lane = threadIdx.x & 31u;
+    const float n_l = lane < nranks ? (float)min(hidden - (int)lane * slice, slice) : 0.0f;
+    const float inv_n_l = lane < nranks ? 1.0f / n_l : 0.0f;
     // After a copy time-out this CTA stops waiting for and issuing copies but
     // still runs every row and every exchange, so its peers never wait on it.
     bool failed = false;
@@ -473,7 +479,7 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
             if (threadIdx.x == 0) atomicOr(err, TF_DEVERR_PRODUCER_WAIT);
         }
         // this slice's own mean and sum of squared deviations from it ...
-        const float mean_c = total / (float)width;
+        const float mean_c = total * inv_w;
         float sq = 0.0f;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -487,16 +493,19 @@ __global__ void __launch_bounds__(MAXT, 512 / MAXT > 0 ? 512 / MAXT : 1) layerno
         }
         exchange(total, cta_sum_alt(sq, red[1]), pb, xpar);
         // ... merged over the slices (Chan et al.'s pairwise update):
-        // M2 = sum_r M2_r + sum_r n_r (mean_r - mean)^2, in rank order
-        float tsum = 0.0f;
-        for (uint32_t r = 0; r < nranks; ++r) tsum += slot[pb][r].x;
+        // M2 = sum_r M2_r + sum_r n_r (mean_r - mean)^2.  Lane r of every warp
+        // takes rank r's terms and the warp sums them with the same shuffle
+        // butterfly (each level adds the same two values in either lane), so
+        // every thread of the cluster gets the same mean and M2.
+        const float2 pr = lane < nranks ? slot[pb][lane] : make_float2(0.0f, 0.0f);
+        float tsum = pr.x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
         const float mean = tsum * inv_h;
-        float m2 = 0.0f;
-        for (uint32_t r = 0; r < nranks; ++r) {
-            const float n_r = (float)min(hidden - (int)r * slice, slice);
-            const float d = slot[pb][r].x / n_r - mean;
-            m2 += slot[pb][r].y + n_r * d * d;
-        }
+        const float dl = pr.x * inv_n_l - mean;
+        float m2 = lane < nranks ? fmaf(n_l * dl, dl, pr.y) : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
         const float rstd = rsqrtf(m2 * inv_h + eps);
         __half *yr = y + row * hidden + c0;
 #pragma unroll
