@@ -31,13 +31,22 @@ __device__ __forceinline__ float epilogue(float acc, int co, const float *scale,
 // ---------------------------------------------------------------- direct
 
 // One thread per output element y[n][oh][ow][co]; co is the fastest index so a
-// warp's x reads are broadcasts and its y writes are contiguous.  The filter
-// taps are taken in batches of kTapBatch: for each 8-channel chunk, the
-// batch's x and filter vectors are all loaded (zeros where a tap lies in the
-// padding) before the first FMA, so a thread waits for memory once per batch
-// and chunk rather than once per tap (a 3x3 filter is one batch).
-constexpr int kTapBatch = 9;
+// warp's x reads are broadcasts and its y writes are contiguous.
+//
+// BATCHED: the K loop runs over units of one filter tap and 8 input channels
+// (one 16-byte x vector and one filter vector), kBatch units at a time, and a
+// batch's vectors are all loaded (zeros where the tap lies in the padding)
+// before its first FMA: a thread waits for memory once per batch (a 3x3 filter
+// over 8 input channels is one batch).  That pays where each thread's
+// reduction is a few taps of few channels and there are few threads (small
+// 3x3 layers: the tiny workload's 1x16x16, 8 -> 16 takes 2.5 us against 4.2);
+// with more threads, or long channel runs per tap, the registers it holds cost
+// more occupancy than its loads gain, and the tap-by-tap loop (whose channel
+// loop the compiler unrolls) is faster.  Batched layers have fewer than 2^31
+// outputs by construction (see launch_conv_direct).
+constexpr int kBatch = 9;
 
+template <bool BATCHED>
 __global__ void __launch_bounds__(256) conv_direct_kernel(ConvArgs a)
 {
     pdl_begin();
@@ -45,58 +54,76 @@ __global__ void __launch_bounds__(256) conv_direct_kernel(ConvArgs a)
     const int64_t total = (int64_t)s.N * a.Ho * a.Wo * s.C_out;
     const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (o >= total) return;
-    int co, ow, oh, n;
-    if (total <= 0x7fffffff) {   // 32-bit index arithmetic when it suffices
+    float acc = 0.0f;
+    int co;
+    if constexpr (BATCHED) {
+        // (launched only for small layers: 32-bit output index)
         int r = (int)o;
         co = r % s.C_out;
         r /= s.C_out;
-        ow = r % a.Wo;
+        const int ow = r % a.Wo;
         r /= a.Wo;
-        oh = r % a.Ho;
-        n = r / a.Ho;
-    } else {
-        int64_t r = o;
-        co = (int)(r % s.C_out);
-        r /= s.C_out;
-        ow = (int)(r % a.Wo);
-        r /= a.Wo;
-        oh = (int)(r % a.Ho);
-        n = (int)(r / a.Ho);
-    }
-    const uint4 *x = reinterpret_cast<const uint4 *>(a.x);
-    const int cch = s.C_in / 8;   // 16-byte chunks per pixel and per filter tap
-    const uint4 *w = reinterpret_cast<const uint4 *>(a.w) + (int64_t)co * s.KH * s.KW * cch;
-    const int taps = s.KH * s.KW;
-    const int ih0 = oh * s.stride_h - s.pad_h, iw0 = ow * s.stride_w - s.pad_w;
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    float acc = 0.0f;
-    for (int t0 = 0; t0 < taps; t0 += kTapBatch) {
-        int kh = t0 / s.KW, kw = t0 - (t0 / s.KW) * s.KW;
-        int64_t xoff[kTapBatch];   // first chunk of the tap's input pixel; -1 in the padding
+        const int oh = r % a.Ho;
+        const int n = r / a.Ho;
+        const uint4 *x = reinterpret_cast<const uint4 *>(a.x);
+        const int cch = s.C_in / 8;   // 16-byte chunks per pixel and per filter tap
+        const int units = s.KH * s.KW * cch;
+        const uint4 *w = reinterpret_cast<const uint4 *>(a.w) + (int64_t)co * units;   // unit u at w[u]
+        const int ih0 = oh * s.stride_h - s.pad_h, iw0 = ow * s.stride_w - s.pad_w;
+        const int64_t img = (int64_t)n * s.H;
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+        int kh = 0, kw = 0, c = 0;   // the next unit's tap and chunk
+        for (int u0 = 0; u0 < units; u0 += kBatch) {
+            uint4 xv[kBatch], wv[kBatch];
 #pragma unroll
-        for (int j = 0; j < kTapBatch; ++j) {
-            const int ih = ih0 + kh, iw = iw0 + kw;
-            const bool in = t0 + j < taps && (unsigned)ih < (unsigned)s.H && (unsigned)iw < (unsigned)s.W;
-            xoff[j] = in ? (((int64_t)n * s.H + ih) * s.W + iw) * cch : -1;
-            if (++kw == s.KW) {
-                kw = 0;
-                ++kh;
-            }
-        }
-        for (int c = 0; c < cch; ++c) {
-            uint4 xv[kTapBatch], wv[kTapBatch];
-#pragma unroll
-            for (int j = 0; j < kTapBatch; ++j) {
-                xv[j] = xoff[j] >= 0 ? __ldg(x + xoff[j] + c) : zero;
-                wv[j] = xoff[j] >= 0 ? __ldg(w + (int64_t)(t0 + j) * cch + c) : zero;
+            for (int j = 0; j < kBatch; ++j) {
+                const int ih = ih0 + kh, iw = iw0 + kw;
+                const bool in = u0 + j < units && (unsigned)ih < (unsigned)s.H && (unsigned)iw < (unsigned)s.W;
+                xv[j] = in ? __ldg(x + ((img + ih) * s.W + iw) * cch + c) : zero;
+                wv[j] = in ? __ldg(w + u0 + j) : zero;
+                if (++c == cch) {
+                    c = 0;
+                    if (++kw == s.KW) {
+                        kw = 0;
+                        ++kh;
+                    }
+                }
             }
 #pragma unroll
-            for (int j = 0; j < kTapBatch; ++j) {
+            for (int j = 0; j < kBatch; ++j) {
+                if (u0 + j >= units) break;
                 float xf[8], wf[8];
                 bf8(xv[j], xf);
                 bf8(wv[j], wf);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) acc = fmaf(xf[k], wf[k], acc);
+            }
+        }
+    } else {
+        int64_t r = o;
+        co = (int)(r % s.C_out);
+        r /= s.C_out;
+        const int ow = (int)(r % a.Wo);
+        r /= a.Wo;
+        const int oh = (int)(r % a.Ho);
+        const int n = (int)(r / a.Ho);
+        const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(a.x);
+        const __nv_bfloat16 *w = reinterpret_cast<const __nv_bfloat16 *>(a.w) + (int64_t)co * s.KH * s.KW * s.C_in;
+        for (int kh = 0; kh < s.KH; ++kh) {
+            const int ih = oh * s.stride_h - s.pad_h + kh;
+            if (ih < 0 || ih >= s.H) continue;
+            for (int kw = 0; kw < s.KW; ++kw) {
+                const int iw = ow * s.stride_w - s.pad_w + kw;
+                if (iw < 0 || iw >= s.W) continue;
+                const uint4 *xp = reinterpret_cast<const uint4 *>(x + (((int64_t)n * s.H + ih) * s.W + iw) * s.C_in);
+                const uint4 *wp = reinterpret_cast<const uint4 *>(w + ((int64_t)kh * s.KW + kw) * s.C_in);
+                for (int c = 0; c < s.C_in / 8; ++c) {
+                    float xf[8], wf[8];
+                    bf8(__ldg(xp + c), xf);
+                    bf8(__ldg(wp + c), wf);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc = fmaf(xf[j], wf[j], acc);
+                }
             }
         }
     }
@@ -180,7 +207,12 @@ cudaError_t launch_conv_direct(const ConvArgs &a, cudaStream_t st)
     const int64_t total = (int64_t)a.s.N * a.Ho * a.Wo * a.s.C_out;
     const int64_t grid = (total + 255) / 256;
     if (grid > 0x7fffffff) return cudaErrorNotSupported;
-    return launch_pdl(conv_direct_kernel, dim3((unsigned)grid), dim3(256), 0, st, a);
+    // batched tap loads for small layers with several taps of few channels
+    // (measured crossovers on GB300: from ~128K outputs or 64 input channels
+    // on, the tap-by-tap loop is as fast or faster)
+    const bool batched = a.s.KH * a.s.KW > 1 && a.s.C_in < 64 && total < 131072;
+    if (batched) return launch_pdl(conv_direct_kernel<true>, dim3((unsigned)grid), dim3(256), 0, st, a);
+    return launch_pdl(conv_direct_kernel<false>, dim3((unsigned)grid), dim3(256), 0, st, a);
 }
 
 cudaError_t launch_conv_tiled(const ConvArgs &a, cudaStream_t st)

@@ -125,6 +125,10 @@ int select_variant(const tf_conv_shape &s, int Ho, int Wo)
     const bool cin_tail = s.C_in % 64 != 0;
     const bool plain = s.KH == 1 && s.KW == 1 && s.stride_h == 1 && s.stride_w == 1 && s.pad_h == 0 &&
                        s.pad_w == 0;
+    // small layers of several taps over few input channels: the direct
+    // kernel's batched loads (one memory round trip per thread) beat the
+    // tensor-core kernel's fill up to ~32K outputs
+    if (s.KH * s.KW > 1 && s.C_in < 64 && M * s.C_out <= 32768) return TF_CONV_DIRECT;
     bool tc = conv_umma_supports(s, Ho, Wo);
     if (s.C_in < 16)
         tc = tc && flops >= 15.0e6 && s.C_out >= (plain ? 16 : 48);

@@ -141,6 +141,9 @@ def test_dispatch_selects_by_shape(native_lib):
     # few input channels and few outputs stay on the CUDA cores
     assert sel(synth.ConvShape(4, 32, 32, 8, 32, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_DIRECT
     assert sel(synth.ConvShape(16, 64, 64, 8, 32, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_TILED
+    # small 3x3 layers over few input channels: the direct kernel's batched tap loads
+    assert sel(synth.ConvShape(1, 16, 16, 24, 128, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_DIRECT
+    assert sel(synth.ConvShape(4, 32, 32, 24, 16, 3, 3, (1, 1), (1, 1))) == b.TF_CONV_UMMA   # 64K outputs
     # tiny reductions stay on the direct kernel even when the tensor-core one could run
     assert sel(synth.ConvShape(1, 16, 16, 64, 64, 1, 1)) == b.TF_CONV_DIRECT
     assert sel(synth.ConvShape(1, 16, 16, 256, 64, 1, 1)) == b.TF_CONV_UMMA
