@@ -85,6 +85,13 @@ CUDA_CORE_SHAPES = [
     synth.ConvShape(1, 11, 13, 24, 5, 5, 3, (2, 1), (2, 1)),     # stride, non-square kernel and pads
     synth.ConvShape(3, 6, 6, 8, 33, 1, 1, (1, 1), (0, 0)),
     synth.ConvShape(1, 20, 20, 8, 16, 7, 7, (1, 1), (3, 3)),
+    # the direct kernel's batched form: a last batch of 7 of 25 units (5x5, 8
+    # channels), 45 units over 40 channels at stride 2, and both sides of its
+    # 128K-output bound (4x32x32x24 -> 16 batched, -> 32 tap by tap)
+    synth.ConvShape(1, 12, 12, 8, 16, 5, 5, (1, 1), (2, 2)),
+    synth.ConvShape(2, 16, 16, 40, 24, 3, 3, (2, 2), (1, 1)),
+    synth.ConvShape(4, 32, 32, 24, 16, 3, 3, (1, 1), (1, 1)),
+    synth.ConvShape(4, 32, 32, 24, 32, 3, 3, (1, 1), (1, 1)),
 ]
 
 
