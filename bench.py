@@ -245,8 +245,9 @@ class Runner:
             self.host_y = torch.empty((rows, hidden), dtype=torch.float16).pin_memory()
         self.nsets = len(self.sets)
 
-    # one fused call on buffer set i: returns the number of our kernels launched
-    def fused(self, i: int) -> int:
+    # one fused call on buffer set i (time_loop counts the kernels it launches
+    # with the library's own launch counter)
+    def fused(self, i: int) -> None:
         b, s, w = self.b, self.sets[i % self.nsets], self.w
         if w.kind == "conv":
             b.tf_conv2d_bn_silu(s["x"], self.wt, self.scale, self.bias, s["y"], self.shape)
@@ -256,41 +257,38 @@ class Runner:
             b.tf_bias_gelu_rowsum(s["x"], self.bias, s["y"], self.rowsum, w.rows, w.cols)
         else:
             b.tf_residual_layernorm(s["a"], s["r"], self.gamma, self.beta, s["y"], w.rows, w.cols, w.eps)
-        return 1
 
-    def unfused(self, i: int) -> int:
+    def unfused(self, i: int) -> None:
         b, s, w = self.b, self.sets[i % self.nsets], self.w
         if w.kind == "conv":
             c = w.conv
             b.tf_unfused_conv2d(s["x"], self.wt, self.t1, self.shape)
             b.tf_unfused_bn(self.t1, self.scale, self.bias, self.t2, c.M, c.C_out)
             b.tf_unfused_silu(self.t2, s["y"], c.M * c.C_out)
-            return 3
+            return
         if w.kind == "bias_gelu":
             b.tf_unfused_bias_add(s["x"], self.bias, self.t, w.rows, w.cols)
             b.tf_unfused_gelu(self.t, s["y"], w.rows * w.cols)
-            return 2
+            return
         if w.kind == "bias_gelu_rowsum":
             b.tf_bias_gelu(s["x"], self.bias, s["y"], w.rows, w.cols)
             b.tf_unfused_rowsum(s["y"], self.rowsum, w.rows, w.cols)
-            return 2
+            return
         b.tf_unfused_residual_add(s["a"], s["r"], self.s, w.rows * w.cols)
         b.tf_unfused_layernorm(self.s, self.n, w.rows, w.cols, w.eps)
         b.tf_unfused_affine(self.n, self.gamma, self.beta, s["y"], w.rows, w.cols)
-        return 3
 
     # end to end through the C ABI from pinned host buffers: H2D of the step's
     # inputs, the fused call, D2H of the result
-    def e2e(self, i: int) -> int:
+    def e2e(self, i: int) -> None:
         s = self.sets[i % self.nsets]
         if self.w.kind == "layernorm":
             s["a"].copy_(self.host_a, non_blocking=True)
             s["r"].copy_(self.host_r, non_blocking=True)
         else:
             s["x"].copy_(self.host_x, non_blocking=True)
-        k = self.fused(i)
+        self.fused(i)
         self.host_y.copy_(s["y"].view(self.host_y.shape), non_blocking=True)
-        return k
 
 
 def time_e2e_pipelined(r: "Runner", steps: int, warmup: int, world: int) -> float:
@@ -376,27 +374,26 @@ class PairRunner:
         b, s = self.b, self.sets[i % self.nsets]
         b.tf_conv2d_bn_silu(s["x"], self.w1, self.s1, self.b1, s["u"], self.sh1)
         b.tf_conv2d_bn_silu(s["u"], self.w2, self.s2, self.b2, s["y"], self.sh2)
-        return 2
 
     def standalone(self, i):
         b, s = self.b, self.sets[i % self.nsets]
         b.tf_unfused_conv2d(s["x"], self.w1, self.t, self.sh1)
         self.activation(i)
         b.tf_conv2d_bn_silu(s["u"], self.w2, self.s2, self.b2, s["y"], self.sh2)
-        return 4
 
     def activation(self, i):
         b, s = self.b, self.sets[i % self.nsets]
         b.tf_unfused_bn(self.t, self.s1, self.b1, self.t2, self.p.M, self.p.C_out)
         b.tf_unfused_silu(self.t2, s["u"], self.u_elems)
-        return 2
 
 
 def time_loop(fn, steps: int, warmup: int, world: int, clocks=None):
     """Times exactly `steps` calls of fn(i) with CUDA events on the current
     stream, bracketed by a barrier and a device synchronise on both sides;
-    returns (max-over-ranks ms per step, kernels launched in the timed region)."""
+    returns (max-over-ranks ms per step, kernels launched in the timed region:
+    the library's own launch counter, read on both sides of the timed calls)."""
     import torch
+    from gemm_conv_epilogues_gb300 import binding as b
     for i in range(warmup):
         fn(i)
     torch.cuda.synchronize()
@@ -404,13 +401,14 @@ def time_loop(fn, steps: int, warmup: int, world: int, clocks=None):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches = 0
     ctx = clocks if clocks is not None else _Null()
     with ctx:
+        c0 = b.tf_launch_count()
         ev0.record(stream)
         for i in range(steps):
-            launches += fn(warmup + i)
+            fn(warmup + i)
         ev1.record(stream)
+        launches = b.tf_launch_count() - c0
         torch.cuda.synchronize()
     barrier(world)
     ms = ev0.elapsed_time(ev1) / steps

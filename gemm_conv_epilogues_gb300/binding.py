@@ -67,6 +67,7 @@ _SIGS = {
     "tf_get_wait_limit_ns": ([], _u64),
     "tf_read_device_error": ([ctypes.POINTER(ctypes.c_uint32)], _i),
     "tf_wait_probe": ([_u64, _vp], _i),
+    "tf_launch_count": ([], _u64),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -225,6 +226,11 @@ def tf_set_wait_limit_ns(limit_ns: int) -> None:
 
 def tf_get_wait_limit_ns() -> int:
     return int(_lib.tf_get_wait_limit_ns())
+
+
+def tf_launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(_lib.tf_launch_count())
 
 
 def tf_read_device_error():

@@ -89,6 +89,7 @@ struct UmmaParams {
     uint32_t *err;
     uint64_t wait_ns;
     int M, C_out, KW, HoWo, Wo;
+    int m_base;              // first output row of this launch's tiles (a wide kernel's tail launch)
     int stride_h, stride_w, pad_h, pad_w;
     int num_kb, cblocks, num_n_tiles, num_tiles;
     int epilogue;            // 0: plain bf16 store, 1: BN + SiLU, 2: fp32 split-K partial to ws
@@ -238,7 +239,8 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
                 const int kb_begin = work < p.split_from ? (work - tile * p.splits) * p.kb_per_split : 0;
                 const int kb_end = min(kb_begin + p.kb_per_split, p.num_kb);
                 const int mh = MH > 1 && part >= 0 ? 1 : MH;   // 128-row halves this item loads
-                const int m0 = ((tile / p.num_n_tiles) * CL + crank) * (BM * MH) + (MH > 1 && part > 0 ? part * BM : 0);
+                const int m0 = p.m_base + ((tile / p.num_n_tiles) * CL + crank) * (BM * MH) +
+                               (MH > 1 && part > 0 ? part * BM : 0);
                 const int n0 = (tile % p.num_n_tiles) * BN;
                 int img[MH], w_base[MH], h_base[MH];
 #pragma unroll
@@ -440,7 +442,8 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
             const bool npart = MH == 1 && part >= 0;          // a part along the channels
             const int mh = MH > 1 && part >= 0 ? 1 : MH;     // 128-row halves of this item
             const int width = npart ? BN / p.parts : BN;       // channels of this item
-            const int m0 = ((tile / p.num_n_tiles) * CL + crank) * (BM * MH) + (MH > 1 && part > 0 ? part * BM : 0);
+            const int m0 = p.m_base + ((tile / p.num_n_tiles) * CL + crank) * (BM * MH) +
+                           (MH > 1 && part > 0 ? part * BM : 0);
             const int tile_n0 = (tile % p.num_n_tiles) * BN;
             const int n0 = tile_n0 + (npart && part > 0 ? part * width : 0);
             // First output channel of accumulator columns [32c, 32c+32).  A part of
@@ -680,6 +683,28 @@ inline void split_wide_tail(UmmaParams &p, int units)
     }
 }
 
+// The last, partial wave of wide tiles, when it fills at most half the units,
+// left to a second launch on 128-row tiles: on its own ring plan (one MMA per
+// K step, more stages) such a tile keeps the tensor pipe fed, where the wide
+// kernel's 128-row halves (48 KB stages carrying one MMA each) starve it.  The
+// launch keeps whole 256-row blocks of tiles (all their channel tiles); false
+// (and no change) when there is no such tail or no block would be left.
+template <int CL, int MH>
+bool leave_wide_tail(UmmaParams &p, int units, int *tail_row)
+{
+    if (!tail_row) return false;
+    const int rem = p.num_tiles % units;
+    if (rem == 0 || 2 * rem > units) return false;
+    const int blocks = (p.num_tiles - rem) / p.num_n_tiles;   // 256-row blocks (per CTA) kept here
+    if (blocks < 1) return false;
+    p.num_tiles = blocks * p.num_n_tiles;
+    p.num_work = p.num_tiles;
+    p.split_from = p.num_work;
+    p.parts = 1;
+    *tail_row = p.m_base + blocks * CL * BM * MH;
+    return true;
+}
+
 // The last, partial wave of tiles with a resident filter block and one
 // channel tile as quarter or half tiles over 4 or 2 times the units, when that
 // still fits in one wave; each part is at least `min_width` channels wide
@@ -697,9 +722,13 @@ inline void split_channel_tail(UmmaParams &p, int units, int bn, int min_width)
     }
 }
 
+// With MH = 2 and tail_row given, a last partial wave of at most half the
+// units is left out of this launch (whole 256-row blocks of tiles) and
+// *tail_row set to its first output row, for the caller to run on 128-row
+// tiles in a second launch; *tail_row stays 0 when this launch covers all.
 template <int BN, bool IM2COL, int CL, int EPI, int MH = 1, int CG = 1>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty, UmmaParams p,
-                      bool want_bres, cudaStream_t st)
+                      bool want_bres, cudaStream_t st, int *tail_row = nullptr)
 {
     constexpr int kThreads = threads_for(EPI);
     auto kern = conv_umma_kernel<BN, IM2COL, CL, EPI, MH, CG>;
@@ -740,13 +769,13 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         // channel tile c % num_n_tiles
         if (p.sm.b_res) grid = grid / p.num_n_tiles * p.num_n_tiles;
         if (grid < 1) return cudaErrorNotSupported;
-        if (MH > 1) split_wide_tail(p, grid);
+        if (MH > 1 && !leave_wide_tail<CL, MH>(p, grid, tail_row)) split_wide_tail(p, grid);
         if (MH == 1 && p.sm.b_res && p.num_n_tiles == 1 && p.C_out == BN && p.splits == 1)
             split_channel_tail(p, grid, BN, 32);
         if (grid > p.num_work) grid = p.num_work;
         cfg.gridDim = dim3((unsigned)grid);
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
+        return counted(cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p));
     } else {
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = CL;
@@ -763,14 +792,14 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
         // a resident filter block pins each pair to one channel tile
         if (p.sm.b_res) clusters = clusters / p.num_n_tiles * p.num_n_tiles;
         if (clusters < 1) return cudaErrorNotSupported;
-        if (MH > 1) split_wide_tail(p, clusters);
+        if (MH > 1 && !leave_wide_tail<CL, MH>(p, clusters, tail_row)) split_wide_tail(p, clusters);
         // a part of a paired MMA takes half its channels from each CTA's half
         // of the block, in whole 32-channel chunks: parts of >= 64 channels
         if (MH == 1 && p.sm.b_res && p.num_n_tiles == 1 && p.C_out == BN && p.splits == 1)
             split_channel_tail(p, clusters, BN, 64);
         if (clusters > p.num_work) clusters = p.num_work;
         cfg.gridDim = dim3(CL * clusters);
-        return cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
+        return counted(cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p));
     }
 }
 
@@ -914,6 +943,7 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     p.err = device_error_word();
     p.wait_ns = wait_limit_ns();
     p.M = (int)M;
+    p.m_base = 0;
     p.C_out = s.C_out;
     p.KW = s.KW;
     p.HoWo = a.Ho * a.Wo;
@@ -943,12 +973,30 @@ cudaError_t launch_conv_umma(const ConvArgs &a, cudaStream_t st)
     p.parts = 1;
     if (p.err == nullptr) return cudaErrorInitializationError;
     const bool want_bres = p.splits == 1;
-    if (a.wide && pair)
-        return im2col ? launch_bn<256, true, 2, kEpiWarpsLongK, 2, 2>(ta, tb, ty, p, false, st)
-                      : launch_bn<256, false, 2, kEpiWarpsLongK, 2, 2>(ta, tb, ty, p, false, st);
-    if (a.wide)
-        return im2col ? launch_bn<256, true, 1, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st)
-                      : launch_bn<256, false, 1, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st);
+    if (a.wide) {
+        // the wide kernel, then (when it leaves one) its partial last wave on
+        // 128-row tiles of the same CTA grouping
+        int tail_row = 0;
+        cudaError_t e;
+        if (pair)
+            e = im2col ? launch_bn<256, true, 2, kEpiWarpsLongK, 2, 2>(ta, tb, ty, p, false, st, &tail_row)
+                       : launch_bn<256, false, 2, kEpiWarpsLongK, 2, 2>(ta, tb, ty, p, false, st, &tail_row);
+        else
+            e = im2col ? launch_bn<256, true, 1, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st, &tail_row)
+                       : launch_bn<256, false, 1, kEpiWarpsLongK, 2>(ta, tb, ty, p, false, st, &tail_row);
+        if (e != cudaSuccess || tail_row == 0) return e;
+        UmmaParams t = p;
+        t.m_base = tail_row;
+        t.num_tiles = (int)((((int64_t)M - tail_row + BM - 1) / BM + cl - 1) / cl) * t.num_n_tiles;
+        t.num_work = t.num_tiles;
+        t.split_from = t.num_work;
+        t.parts = 1;
+        if (pair)
+            return im2col ? launch_bn<256, true, 2, kEpiWarpsLongK, 1, 2>(ta, tb, ty, t, false, st)
+                          : launch_bn<256, false, 2, kEpiWarpsLongK, 1, 2>(ta, tb, ty, t, false, st);
+        return im2col ? launch_bn<256, true, 1, kEpiWarpsLongK, 1>(ta, tb, ty, t, false, st)
+                      : launch_bn<256, false, 1, kEpiWarpsLongK, 1>(ta, tb, ty, t, false, st);
+    }
     if (pair)
         return im2col ? launch_im<true, 2, 2>(bn, ta, tb, ty, p, want_bres, st)
                       : launch_im<false, 2, 2>(bn, ta, tb, ty, p, want_bres, st);
@@ -1048,7 +1096,7 @@ cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t st)
     uint32_t *err = device_error_word();
     if (err == nullptr) return cudaErrorInitializationError;
     wait_probe_kernel<<<1, 32, 0, st>>>(err, limit_ns);
-    return cudaGetLastError();
+    return counted(cudaGetLastError());
 }
 
 }  // namespace tf

@@ -655,9 +655,9 @@ cudaError_t launch_ln_cluster_with(const void *a, const void *b, const float *ga
     }
     if (clusters > rows) clusters = (int)rows;
     cfg.gridDim = dim3((unsigned)(clusters * csize));
-    return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const __half *>(a), reinterpret_cast<const __half *>(b),
+    return counted(cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const __half *>(a), reinterpret_cast<const __half *>(b),
                               gamma, beta, reinterpret_cast<__half *>(y), rows, (int)hidden, (int)slice, eps, stages,
-                              err, wait_limit_ns());
+                              err, wait_limit_ns()));
 }
 
 template <bool RESIDUAL, bool AFFINE>

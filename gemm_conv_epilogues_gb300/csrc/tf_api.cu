@@ -14,6 +14,8 @@ static __device__ uint32_t g_tf_device_error;
 
 namespace tf {
 
+std::atomic<unsigned long long> g_launch_count{0};
+
 static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
@@ -385,6 +387,8 @@ int tf_unfused_affine(const void *nrm, const float *gamma, const float *beta, vo
 void tf_set_wait_limit_ns(uint64_t limit_ns) { g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed); }
 
 uint64_t tf_get_wait_limit_ns(void) { return wait_limit_ns(); }
+
+uint64_t tf_launch_count(void) { return tf::g_launch_count.load(std::memory_order_relaxed); }
 
 int tf_read_device_error(uint32_t *word)
 {

@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stdint.h>
 
 #include "tf_epilogue.h"
@@ -110,6 +112,15 @@ __device__ __forceinline__ int cta_sync_and(int pred)
     return __syncthreads_and(pred);
 }
 
+// Kernels launched by this library in this process (tf_launch_count);
+// every launch site passes its cudaLaunchKernelEx result through counted().
+extern std::atomic<unsigned long long> g_launch_count;
+inline cudaError_t counted(cudaError_t e)
+{
+    if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+    return e;
+}
+
 // kern<<<grid, block, smem, st>>>(args...) with programmatic dependent launch allowed.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args)
@@ -124,7 +135,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    return counted(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...));
 }
 
 __device__ __forceinline__ float ex2_approx(float x)

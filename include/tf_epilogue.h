@@ -305,6 +305,13 @@ uint64_t tf_get_wait_limit_ns(void);
  * failed.  Not for use inside stream capture. */
 int tf_read_device_error(uint32_t *word);
 
+/* Number of kernels this library has launched in this process so far (every
+ * entry point, every device and stream; launches the runtime accepted).  One
+ * call may launch more than one kernel: tf_conv2d_bn_silu runs a wide-tile
+ * kernel and then its partial last wave on 128-row tiles, the split-K path
+ * adds a reduction.  For benchmarks that report how many kernels ran. */
+uint64_t tf_launch_count(void);
+
 /* Launches one small kernel that waits, with the given limit, on an mbarrier
  * that nothing ever arrives on; it gives up, sets TF_DEVERR_PROBE_WAIT and
  * returns.  Exercises the time-out path without disturbing the GPU. */

@@ -33,6 +33,13 @@ def test_library_exports_every_declared_symbol(native_lib):
         assert hasattr(native_lib, n)
 
 
+def test_launch_counter_counts_nothing_rejected_on_the_host(native_lib):
+    from gemm_conv_epilogues_gb300 import binding as b
+    n0 = b.tf_launch_count()
+    assert b.tf_bias_gelu(0, 0, 0, 8, 8, 0, check=False) == b.TF_ERR_INVALID_ARG
+    assert b.tf_launch_count() == n0
+
+
 def test_status_strings(native_lib):
     from gemm_conv_epilogues_gb300 import binding as b
     assert b.status_string(0) == "TF_OK"

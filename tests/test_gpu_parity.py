@@ -232,6 +232,32 @@ def test_conv_umma_wide_two_waves_sampled(b):
     _assert_no_device_error(b)
 
 
+# One wave of wide tiles and a few more: the few (at most half a wave) run as
+# a second launch on 128-row tiles, from the first row the wide launch leaves
+# (ragged M: 11 x 61 x 61 = 40931 pixels).  Every output is checked.
+WIDE_TAIL_SHAPES = [
+    synth.ConvShape(11, 61, 61, 64, 256, 3, 3, (1, 1), (1, 1)),
+    synth.ConvShape(11, 61, 61, 128, 256, 1, 1, (1, 1), (0, 0)),
+]
+
+
+@pytest.mark.parametrize("variant", [4, 5], ids=["pair", "cta"])
+@pytest.mark.parametrize("c", WIDE_TAIL_SHAPES, ids=["3x3", "1x1"])
+def test_conv_umma_wide_tail_launch(b, c, variant):
+    d = synth.conv_inputs(c, seed=18, w_dist="normal_fanin")
+    n0 = b.tf_launch_count()
+    got = _run_conv(b, c, d, variant)
+    conv_kernels = b.tf_launch_count() - n0 - 1   # less the filter pack
+    # 80 pair tiles (160 single-CTA tiles): two launches on a GPU whose pairs
+    # (CTAs) leave a partial wave of at most half, as GB300's do
+    assert conv_kernels in (1, 2)
+    if torch.cuda.get_device_properties(0).multi_processor_count >= 148:
+        assert conv_kernels == 2
+    ref = oracle.conv2d_bn_silu(d["x"], d["w_oihw"], d["scale"], d["bias"], c.stride, c.pad)
+    _conv_check(got, ref)
+    _assert_no_device_error(b)
+
+
 def test_conv_umma_wide_rejects_other_channel_counts(b):
     c = synth.ConvShape(1, 12, 12, 64, 128, 3, 3, (1, 1), (1, 1))
     x = torch.zeros((c.N, c.H, c.W, c.C_in), dtype=torch.int16, device="cuda")
