@@ -120,15 +120,18 @@ int tf_pack_filter_nhwc(const void *w_oihw, void *w_ohwi,
  * accumulated in fp32.  Requires C_in % 8 == 0 and 16-byte aligned x, w, y;
  * shapes that go to a tensor-core kernel also need 16-byte aligned scale and
  * bias (TF_ERR_UNSUPPORTED otherwise).  The kernel is chosen by shape (see
- * tf_conv2d_bn_silu_select). */
+ * tf_conv2d_bn_silu_select); the wide-tile kernels may be followed by a
+ * second launch on the same stream that computes the rows of their last,
+ * partial wave on 128-row tiles (tf_launch_count counts both). */
 int tf_conv2d_bn_silu(const void *x, const void *w_ohwi, const float *scale, const float *bias,
                       void *y, const tf_conv_shape *shape, tf_stream_t stream);
 
 /* Same as tf_conv2d_bn_silu with the kernel forced (TF_CONV_*).  Returns
- * TF_ERR_UNSUPPORTED when the forced kernel cannot take the shape
- * (TF_CONV_UMMA and TF_CONV_UMMA_PAIR need C_in % 64 == 0, C_out % 32 == 0,
- * strides <= 8 and padding <= 128; TF_CONV_UMMA_PAIR_WIDE and TF_CONV_UMMA_WIDE
- * also C_out % 256 == 0). */
+ * TF_ERR_UNSUPPORTED when the forced kernel cannot take the shape (the
+ * tensor-core kernels: strides <= 8 and padding <= 128 for im2col shapes;
+ * TF_CONV_UMMA takes any C_in % 8 == 0 and any C_out, TF_CONV_UMMA_PAIR needs
+ * C_out % 32 == 0, TF_CONV_UMMA_PAIR_WIDE and TF_CONV_UMMA_WIDE
+ * C_out % 256 == 0). */
 int tf_conv2d_bn_silu_variant(const void *x, const void *w_ohwi, const float *scale,
                               const float *bias, void *y, const tf_conv_shape *shape,
                               int variant, tf_stream_t stream);
