@@ -66,12 +66,14 @@ typedef enum {
     TF_CONV_UMMA_PAIR = 3, /* the same on CTA pairs (2-CTA clusters) with the paired MMA
                               (tcgen05 .cta_group::2, M = 256): each CTA loads its own 128 output
                               pixels and HALF of every filter tile, and the two SMs' tensor cores
-                              read both halves; the dispatch's choice for other long reductions
-                              (K > 1024) over at least two waves of tiles */
+                              read both halves; the dispatch's choice for im2col shapes over at
+                              least two waves of pair tiles with C_out % 256 == 0 and at most 16
+                              K steps, or with C_in not a multiple of 64 and C_out >= 64 */
     TF_CONV_UMMA_PAIR_WIDE = 4, /* paired MMA with 256-pixel tiles per CTA: two M = 256 MMAs per K
                                   step read each half filter tile (C_out % 256 == 0 only); the
                                   dispatch's choice for im2col shapes (not plain 1x1 GEMMs) with
-                                  C_out % 256 == 0 and at least a wave of 512-pixel pair tiles */
+                                  C_out % 256 == 0, at least 32 K steps and at least half a wave of
+                                  512-pixel pair tiles */
     TF_CONV_UMMA_WIDE = 5  /* 256-pixel tiles on single CTAs (C_out % 256 == 0 only) */
 } tf_conv_variant;
 
