@@ -72,8 +72,8 @@ typedef enum {
     TF_CONV_UMMA_PAIR_WIDE = 4, /* paired MMA with 256-pixel tiles per CTA: two M = 256 MMAs per K
                                   step read each half filter tile (C_out % 256 == 0 only); the
                                   dispatch's choice for im2col shapes (not plain 1x1 GEMMs) with
-                                  C_out % 256 == 0, at least 32 K steps and at least half a wave of
-                                  512-pixel pair tiles */
+                                  C_out % 256 == 0, at least 32 K steps and at least a wave of
+                                  512-pixel pair tiles (one per CTA pair) */
     TF_CONV_UMMA_WIDE = 5  /* 256-pixel tiles on single CTAs (C_out % 256 == 0 only) */
 } tf_conv_variant;
 
