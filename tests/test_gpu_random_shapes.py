@@ -173,13 +173,16 @@ def test_calls_captured_in_a_cuda_graph(b):
     assert rc == b.TF_OK and word == 0
 
 
-@pytest.mark.parametrize("variant", ["pair", "wide"])
+@pytest.mark.parametrize("variant", ["pair", "wide", "wide_tail_launch"])
 def test_cluster_conv_captured_in_a_cuda_graph(b, variant):
     # the CTA-pair kernels (cluster and programmatic-launch attributes)
-    # captured once and replayed on new inputs, wide tiles with their
-    # half-tile tail
+    # captured once and replayed on new inputs: wide tiles with their
+    # half-tile tail, and a full wave of wide tiles whose partial last wave
+    # is a second launch (two kernels in the graph)
     v = b.TF_CONV_UMMA_PAIR if variant == "pair" else b.TF_CONV_UMMA_PAIR_WIDE
     c = synth.ConvShape(2, 20, 20, 64, 256, 3, 3, (1, 1), (1, 1))
+    if variant == "wide_tail_launch":
+        c = synth.ConvShape(11, 61, 61, 64, 256, 3, 3, (1, 1), (1, 1))
     d0 = synth.conv_inputs(c, seed=80, w_dist="normal_fanin")
     w = torch.empty((c.C_out, c.KH, c.KW, c.C_in), dtype=torch.int16, device="cuda")
     b.tf_pack_filter_nhwc(dev_u16(d0["w_oihw"]), w, c.C_out, c.C_in, c.KH, c.KW)
