@@ -127,8 +127,10 @@ struct UmmaParams {
 // operands per 1024 tensor cycles instead of 48 KB per 512.  Their 256 x BN
 // accumulator fills TMEM at BN = 256, so it is single-buffered: the MMAs of a
 // tile wait for the epilogue of the previous one, a short pause against a
-// long K loop.  Items from split_from on are then the 128-row halves of the
-// last, partial wave's tiles (parts = 2).
+// long K loop.  A last, partial wave of at most half the units goes to a
+// second launch on 128-row tiles (leave_wide_tail); where no full wave
+// precedes it, items from split_from on are instead the 128-row halves of
+// its tiles (parts = 2) in this launch.
 //
 // Paired MMA (CG = 2, on CL = 2 clusters): the two CTAs of a pair run one
 // tcgen05.mma.cta_group::2 of M = 256 (128 rows per CTA, MH of them per K
@@ -672,7 +674,8 @@ bool plan_smem(int num_kb, bool want_bres, SmemPlan &sm)
 }
 
 // The last, partial wave of wide tiles as their 128-row halves over twice the
-// units (CTAs, or CTA pairs), when that still fits in one wave.
+// units (CTAs, or CTA pairs), when that still fits in one wave (used when
+// leave_wide_tail leaves nothing to a second launch).
 inline void split_wide_tail(UmmaParams &p, int units)
 {
     const int rem = p.num_tiles % units;
