@@ -5,8 +5,8 @@
 // "Costs and benefits of kernel fusion", "Worked example: Fusing a residual
 // and normalization chain": load activation and residual once, compute the
 // row statistics, normalise, apply scale and bias, write the final output.
-// One CTA owns one row at a time ("whether one block can own a row efficiently
-// across hidden sizes"): each thread keeps its slice of s = act + res in fp32
+// One CTA owns one row at a time (the page asks how far that stays efficient
+// as the hidden size grows): each thread keeps its slice of s = act + res in fp32
 // registers, the CTA reduces the sum (mean), then the sum of squared
 // deviations from those registers (variance, two-pass), then writes
 // (s - mean) * rsqrt(var + eps) * gamma + beta.  s is never written to HBM.
@@ -328,8 +328,8 @@ __device__ __forceinline__ uint32_t cluster_nctarank()
 // of every CTA streams its slice of the coming rows (act and res) into a
 // shared-memory ring with bulk copies, and each thread holds NV vectors of
 // the current row in fp32 registers, so a row is still read from HBM exactly
-// once ("a hidden width large enough to require a different row-reduction
-// strategy").  Each CTA reduces its slice to
+// once (the page's test of a width too large for one CTA per row).  Each CTA
+// reduces its slice to
 // (sum, M2), M2 the sum of squared deviations from the slice's own mean (two
 // CTA sums), and exchanges that pair once: thread r pushes it into slot
 // [rank] of CTA r with st.async, which completes on CTA r's own mbarrier.
