@@ -685,6 +685,15 @@ def main():
                 attainable = min(peaks["bf16_tflops"], r.flops / r.alg_bytes * peaks["hbm_gbs"] / 1e3)
                 entry.update({"tflops": round(tflops, 1), "frac_tensor": round(tflops / peaks["bf16_tflops"], 4),
                               "frac_attainable": round(tflops / attainable, 4)})
+                if r.w.conv.KH == 1 and r.w.conv.KW == 1:
+                    # what a plain device-to-device copy of the same x -> y bytes,
+                    # over the same rotating sets, takes: the practical bound at
+                    # this transfer size
+                    def copy(i, r=r):
+                        s = r.sets[i % r.nsets]
+                        s["y"].view(-1)[: s["x"].numel()].copy_(s["x"].view(-1))
+                    c_ms, _ = time_loop(copy, steps, args.warmup, world)
+                    entry["copy_ms"] = round(c_ms, 5)
             entry["unf_ms"] = round(u_ms, 5)
             if rank == 0 and world == 1 and not args.no_cpu_baseline:
                 entry["cpu_s"] = cpu_oracle_full(r)["seconds"]
